@@ -1,0 +1,409 @@
+"""Benchmark of the ZeRO shard Adam step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload xl] [--impl gb300|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic inputs
+already resident in HBM: the partition/indexing kernel, the fused
+reduce + overflow test + Adam + fp16 cast kernel over the rank's shard, and the
+device-side commit.  Prints ONE JSON line on rank 0.
+
+N > 1 (launched by torch.distributed.run): every GPU runs an independent
+replica on its own shard (weak scaling, no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Gparams/s and achieved HBM GB/s (% of GB300 peak) of the ZeRO shard Adam step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="xl", help="tiny | gpt2s | ragged | xl | 7b5")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--shard-params", type=int, default=0,
+                    help="shrink the workload to this many params per shard (profiling runs)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers --
+
+def workload(args):
+    from zero_partitioned_mixed_partition_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.shard_params:
+        w = dataclasses.replace(w, name=f"{w.name}-small", numels=(args.shard_params * w.n_d,), align=128)
+    return w
+
+
+def workload_label(w, n_valid):
+    return (f"{w.name}: Psi={w.psi:,} ({len(w.numels)} tensors), N_d={w.n_d}, "
+            f"rank {w.rank} shard of {n_valid:,} params, fp16 grads x{w.n_d} + fp32 master/m/v")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel_source: str):
+    """DRAM bytes per stepped parameter from the committed ncu summary, valid
+    only while the kernel source is unchanged (else None)."""
+    path = os.path.join(ROOT, "profiles", "shard_step_kernel_traffic.txt")
+    try:
+        digest = hashlib.sha256(open(kernel_source, "rb").read()).hexdigest()[:16]
+        vals = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256_16") != digest:
+            return None
+        return {int(k.split("_")[-1]): float(v) for k, v in vals.items() if k.startswith("bytes_per_param_nd_")}
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                   "samples": len(sm)}
+        return out
+
+
+# --------------------------------------------------------------- cpu side ---
+
+def oracle_throughput(w, n_sample: int, seconds: float, threads: int):
+    """Time the oracle, as it stands, on a bounded sample of the workload:
+    n_sample params of the rank's shard, split into contiguous chunks over
+    ``threads`` host threads (ctypes releases the GIL), steps repeated until
+    ``seconds`` have passed.  Returns (Gparams/s, steps, seconds, threads)."""
+    import numpy as np
+    import oracle
+    from zero_partitioned_mixed_partition_gb300 import synth
+
+    oracle.build()
+    contribs = [synth.fp16_bits(synth.grad_contribution(w, n_sample, k, 1, shard=w.rank or 0))
+                for k in range(w.n_d)]
+    master = synth.master_init(w, n_sample, shard=w.rank or 0).numpy()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    params = np.zeros(n_sample, np.uint16)
+    bounds = np.linspace(0, n_sample, threads + 1).astype(np.int64)
+
+    def run_chunk(lo, hi, step):
+        oracle.shard_step([c[lo:hi] for c in contribs], master[lo:hi], m[lo:hi], v[lo:hi], params[lo:hi],
+                          lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                          loss_scale=w.loss_scale, step=step)
+
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        steps += 1
+        ts = [threading.Thread(target=run_chunk, args=(int(bounds[i]), int(bounds[i + 1]), steps))
+              for i in range(threads)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return n_sample * steps / el / 1e9, steps, el, threads
+
+
+def reference_arm(args, rank: int):
+    """The oracle timed on the host cores as the reference arm."""
+    if rank != 0:
+        return
+    w = workload(args)
+    threads = os.cpu_count() or 1
+    n_sample = min(4_000_000, max(w.psi // w.n_d, 1))
+    per_step_s = max(0.5, min(5.0, 60.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(args.warmup):
+        oracle_throughput(w, n_sample, 0.0, threads)
+    vals = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        g, steps, el, th = oracle_throughput(w, n_sample, per_step_s, threads)
+        vals.append(g)
+        if time.perf_counter() - t_all > 180:
+            break
+    value = statistics.median(vals)
+    sample = (f"{n_sample:,} params of the rank's shard x N_d={w.n_d} contributions, "
+              f"{threads} threads over contiguous chunks, >= {per_step_s:.1f} s per step")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Gparams/s",
+            "n_gpus": args.gpus, "steps": len(vals), "warmup": args.warmup,
+            "ms_per_step": round(n_sample / (value * 1e9) * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_label(w, n_sample), "parallelism": "host threads"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "Gparams/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "Gparams/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- gpu side ---
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from zero_partitioned_mixed_partition_gb300 import binding, build
+    from zero_partitioned_mixed_partition_gb300.runner import WorkloadRunner
+
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    binding.lib()
+
+    w = workload(args)
+    if w.rank is not None and world > 1:
+        w = dataclasses.replace(w, rank=(w.rank + rank) % w.n_d)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        run = WorkloadRunner(w, dev, stream=stream)
+        numels_dev = torch.tensor(list(w.numels), dtype=torch.int64, device=dev)
+        lay_scalars = torch.zeros(5, dtype=torch.int64, device=dev)
+        lay_toff = torch.zeros(len(w.numels), dtype=torch.int64, device=dev)
+        lay_soff = torch.zeros(w.n_d + 1, dtype=torch.int64, device=dev)
+        cap = len(w.numels) + w.n_d
+        lay_frags = torch.zeros(cap * 4, dtype=torch.int64, device=dev)
+    torch.cuda.synchronize()
+
+    def one_step(ev_pair=None):
+        binding.zero_partition_layout_device(numels_dev, w.n_d, w.align, lay_scalars, lay_toff, lay_soff,
+                                             lay_frags, cap, stream=stream)
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        for i in range(len(run.views)):
+            run.reduce_adam(i)
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+        run.commit()
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    lay = lay_scalars.cpu().tolist()
+    assert lay[4] == 0 and lay[2] == run.S, lay
+
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = binding.zero_kernel_launches()
+    t_start.record(stream)
+    for k in range(args.steps):
+        one_step(pairs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = binding.zero_kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in pairs]
+    ctrl = run.ctrl_host()
+    assert ctrl["skipped"] == 0 and ctrl["step"] == args.warmup + args.steps, ctrl
+
+    ms_max = ms_total
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    elems = run.elements_per_step()
+    total_elems = elems * world
+    value = total_elems * args.steps / (ms_max / 1e3) / 1e9
+    bytes_step = run.bytes_per_step()
+    hbm_gbs = bytes_step * world * args.steps / (ms_max / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # roofline of the dominant kernel: algorithmic bytes per launch / mean launch time
+    mean_kern_ms = statistics.mean(kern_ms)
+    achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
+    traffic_per_param = recorded_traffic(os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc",
+                                                      "shard_step.cu"))
+    traffic = None
+    if traffic_per_param and w.n_d in traffic_per_param:
+        traffic = round(traffic_per_param[w.n_d] * elems)
+
+    # end to end through the C ABI with host buffers: pinned H2D of the step's
+    # gradient contributions, the step, D2H of the fp16 shard and the control block
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, run, stream, dev, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "Gparams/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
+                   "bytes_per_param": 26 + 2 * w.n_d, "bytes_per_step": bytes_step,
+                   "storage": "fp16 grads and params, fp32 master/m/v (ping-pong)",
+                   "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
+                   if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm_gbs": round(hbm_gbs, 1),
+        "pct_of_nominal_8tbs": round(100 * hbm_gbs / NOMINAL_HBM_GBS, 2),
+        f"pct_of_{peak_kind}_peak": round(100 * hbm_gbs / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "shard_step_kernel", "peak_kind": peak_kind,
+                     "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_min": round(min(kern_ms), 5)},
+        "clocks": clocks,
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        g, steps, el, th = oracle_throughput(w, min(4_000_000, elems), args.cpu_seconds, os.cpu_count() or 1)
+        line["cpu_baseline"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th, "kind": "oracle",
+                                "sample": f"{min(4_000_000, elems):,} params of the shard x N_d={w.n_d}, "
+                                          f"{steps} steps in {el:.1f} s over {th} threads"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def end_to_end(args, run, stream, dev, world):
+    import torch
+    import torch.distributed as dist
+    from zero_partitioned_mixed_partition_gb300 import binding
+
+    r = run.shard_ids[0]
+    n = run.n_valid[r]
+    host_grads = [g[:n].cpu().pin_memory() for g in run.grads[r]]
+    host_params = torch.empty(n, dtype=torch.float16).pin_memory()
+    host_ctrl = torch.empty(run.ctrl.numel(), dtype=torch.int64).pin_memory()
+    h2d = sum(h.numel() * 2 for h in host_grads)
+    d2h = host_params.numel() * 2 + host_ctrl.numel() * 8
+
+    def step():
+        with torch.cuda.stream(stream):
+            for h, g in zip(host_grads, run.grads[r]):
+                g[:n].copy_(h, non_blocking=True)
+            run.step()
+            host_params.copy_(run.state[r][3][:n], non_blocking=True)
+            host_ctrl.copy_(run.ctrl, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    val = run.elements_per_step() * world * args.e2e_steps / (ms / 1e3) / 1e9
+    return {"value": round(val, 3), "unit": "Gparams/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / args.e2e_steps, 4),
+            "path": "pinned host grads -> device (cudaMemcpyAsync), zero_shard_step_async, "
+                    "fp16 shard + control block -> pinned host"}
+
+
+if __name__ == "__main__":
+    main()

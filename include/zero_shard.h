@@ -1,0 +1,253 @@
+/*
+ * zero_shard.h -- C ABI of libzeroshard.so, the GB300 (sm_103a) ZeRO-partitioned
+ * mixed-precision Adam shard step.
+ *
+ * What the library computes, and where it is defined:
+ *   - the partition of the flat parameter index set into N_d disjoint,
+ *     near-equal shards, one per data-parallel rank
+ *     ("DeepSpeed ZeRO Stages", sec. 2 "What 'Partitioning' Means Here";
+ *      sec. 3.2, flat contiguous gradient buffer);
+ *   - the rank's share of the reduce-scatter: its shard of the N_d fp16
+ *     gradient contributions, averaged ("ZeRO Stage 1 Math", "The per-step
+ *     mechanics", beat 2);
+ *   - the elementwise Adam update of the fp32 master weights, m and v of the
+ *     shard and the cast of the shard to fp16 ("DeepSpeed ZeRO Stages",
+ *     sec. 2.1 Fact 1; "ZeRO Stage 1 Math", "Where the 12 bytes come from"
+ *     and "The per-step mechanics", beat 3);
+ *   - the model-state memory per device of stages 0-3 ("DeepSpeed ZeRO
+ *     Stages", sec. 1.2 and 3.1-3.3).
+ * The pages do not describe loss scaling.  The library applies the usual
+ * dynamic-loss-scale rule: the contributions carry a loss scale L that the
+ * step removes, and a non-finite reduced gradient anywhere in the stepped
+ * shards skips the whole step and halves L (never below 1).
+ *
+ * Conventions shared by every entry point:
+ *   - fp16 data is passed as uint16_t bit patterns (IEEE binary16);
+ *   - "DEVICE" pointers are CUDA device (or managed) memory of the current
+ *     device, "HOST" pointers are ordinary host memory;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream);
+ *   - the caller owns every buffer; the library allocates no memory and keeps
+ *     no pointer after a call returns;
+ *   - arguments are checked on the host before anything is enqueued: a bad
+ *     argument returns ZS_ERR_ARG (or ZS_ERR_ALIGN) and launches nothing; a
+ *     CUDA failure returns ZS_ERR_CUDA and zero_last_error() describes it.
+ */
+#ifndef ZERO_SHARD_H_
+#define ZERO_SHARD_H_
+
+#include <stdint.h>
+
+#if defined(_WIN32)
+#define ZS_API
+#else
+#define ZS_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define ZS_OK 0
+#define ZS_ERR_ARG (-1)     /* invalid argument; nothing was enqueued */
+#define ZS_ERR_ALIGN (-2)   /* a pointer is not aligned to its element type */
+#define ZS_ERR_CUDA (-3)    /* a CUDA call failed; see zero_last_error() */
+#define ZS_ERR_TIMEOUT (-4) /* reserved: no kernel of this library waits */
+
+/* Largest data-parallel degree (number of gradient contributions). */
+#define ZS_MAX_ND 1024
+/* Largest number of shards one step may update together. */
+#define ZS_MAX_SHARDS 256
+
+/* One piece of the partition: the overlap of one tensor with one shard. */
+typedef struct zs_fragment {
+    int32_t tensor;        /* index of the tensor in the list */
+    int32_t shard;         /* owning rank */
+    int64_t tensor_offset; /* first element of the piece inside the tensor */
+    int64_t shard_offset;  /* first element of the piece inside the shard */
+    int64_t length;        /* elements, > 0 */
+} zs_fragment;
+
+/* Adam / AdamW hyper-parameters.  weight_decay = 0 gives plain Adam; a
+ * positive value applies decoupled decay: theta -= lr * (u + wd * theta). */
+typedef struct zs_adam {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;
+} zs_adam;
+
+/* One shard of the optimizer state, as one rank owns it.
+ *   grads     HOST array of n_d DEVICE pointers; grads[k] is simulated rank
+ *             k's fp16 gradient for the elements of this shard (scaled by the
+ *             loss scale), >= n values.  The table is read during the call.
+ *   master, m, v
+ *             DEVICE fp32 buffers of >= n values, two sets for ping-pong: a
+ *             step reads set `cur` and writes set `cur ^ 1`, so an overflow
+ *             step can be dropped without a second pass.  Passing the same
+ *             pointer for both sets updates in place; the caller then accepts
+ *             that an overflow step cannot be rolled back.
+ *   params    DEVICE fp16 slice of the full parameter buffer that this shard
+ *             maps to (params_full + rank * shard_numel), >= n values.
+ *   n         elements stepped: the shard's real (non-padding) parameters.
+ *             Elements past n are not read or written.
+ * The vectorised kernel is used when every pointer is 16-byte aligned; any
+ * other 4-byte (fp32) / 2-byte (fp16) aligned layout takes a scalar kernel
+ * with the same arithmetic. */
+typedef struct zs_shard {
+    const uint16_t* const* grads;
+    float* master[2];
+    float* m[2];
+    float* v[2];
+    uint16_t* params;
+    int64_t n;
+} zs_shard;
+
+/* Device-resident step state for the stream-ordered (no host sync) path.
+ * The caller allocates sizeof(zs_ctrl) bytes of 8-byte aligned DEVICE memory
+ * and sets it up with zero_ctrl_init(); the library then owns its contents
+ * between calls.  It may be copied to the host at any time the stream is
+ * idle (for logging or a checkpoint) and copied back to resume. */
+typedef struct zs_ctrl {
+    double loss_scale;     /* L applied to the next step */
+    double beta1_pow;      /* beta1^t for the t committed updates */
+    double beta2_pow;      /* beta2^t */
+    int64_t step;          /* t: committed updates so far */
+    int64_t skipped;       /* steps dropped because of an overflow */
+    int32_t cur;           /* state set (0/1) that holds the committed state */
+    int32_t overflow;      /* OR of the non-finite tests of the step in flight */
+    int32_t last_overflow; /* overflow flag of the last finished step */
+    uint32_t arrivals;     /* internal block counter of the commit kernel; 0 between steps */
+} zs_ctrl;
+
+/* ------------------------------------------------------------------------ */
+/* Partition ("DeepSpeed ZeRO Stages", sec. 2).                              */
+/* ------------------------------------------------------------------------ */
+
+/* Pack n_tensors tensors (HOST numels[], >= 0 each) back to back into one flat
+ * buffer of Psi elements, pad it to Psi_pad = the least multiple of
+ * n_d * align, and cut it into n_d equal shards of S = Psi_pad / n_d
+ * elements; shard i is [i S, (i+1) S).  Outputs (HOST, each may be NULL):
+ *   *psi_out, *psi_padded_out, *shard_numel_out;
+ *   tensor_offsets[n_tensors]  flat offset of each tensor;
+ *   shard_offsets[n_d + 1]     i * S;
+ *   frags[frag_cap]            the tensor/shard overlaps, in flat order
+ *                              (shard-major, tensors in list order);
+ *   *n_frags_out               number of fragments (always written when
+ *                              non-NULL; with frags == NULL this is a count
+ *                              query).  At most n_tensors + n_d - 1.
+ * n_d in [1, ZS_MAX_ND]; align a power of two.  Returns ZS_ERR_ARG for a bad
+ * argument, a negative numel, or frag_cap smaller than the count (in which
+ * case *n_frags_out holds the count needed and frags is left partly filled).
+ * Runs on the host; no CUDA call. */
+ZS_API int32_t zero_partition_layout(const int64_t* numels, int32_t n_tensors, int32_t n_d,
+                                     int32_t align, int64_t* psi_out, int64_t* psi_padded_out,
+                                     int64_t* shard_numel_out, int64_t* tensor_offsets,
+                                     int64_t* shard_offsets, zs_fragment* frags, int64_t frag_cap,
+                                     int64_t* n_frags_out);
+
+/* The same partition computed on the device by one CUDA block, stream-ordered.
+ *   numels_dev[n_tensors]          DEVICE input
+ *   scalars_dev[5]                 DEVICE output: Psi, Psi_pad, S, number of
+ *                                  fragments, status (ZS_OK, or ZS_ERR_ARG when
+ *                                  a numel is negative; the other outputs are
+ *                                  then unspecified)
+ *   tensor_offsets_dev[n_tensors]  DEVICE output (may be NULL if n_tensors = 0)
+ *   shard_offsets_dev[n_d + 1]     DEVICE output
+ *   frags_dev[frag_cap]            DEVICE output or NULL; fragments past
+ *                                  frag_cap are counted but not written
+ *                                  (frag_cap >= n_tensors + n_d - 1 always
+ *                                  suffices).
+ * The results are bit-identical to zero_partition_layout.  Host-side checks
+ * return ZS_ERR_ARG / ZS_ERR_ALIGN (8-byte alignment) before any launch. */
+ZS_API int32_t zero_partition_layout_device(const int64_t* numels_dev, int32_t n_tensors,
+                                            int32_t n_d, int32_t align, int64_t* scalars_dev,
+                                            int64_t* tensor_offsets_dev, int64_t* shard_offsets_dev,
+                                            zs_fragment* frags_dev, int64_t frag_cap, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Model-state memory ("DeepSpeed ZeRO Stages", sec. 1.2, 3.1-3.3).          */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of model state per device for psi parameters on n_d ranks with an
+ * optimizer multiplier k (12 for mixed-precision Adam):
+ *   stage 0: (4 + k) psi          stage 1: 4 psi + k psi / n_d
+ *   stage 2: 2 psi + (2 + k) psi / n_d      stage 3: (4 + k) psi / n_d
+ * Returns NaN for a stage outside 0..3 or n_d < 1.  Host only. */
+ZS_API double zero_state_bytes(double psi, int32_t n_d, int32_t stage, double k);
+
+/* ------------------------------------------------------------------------ */
+/* The shard step.                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* One optimizer step over n_shards shards, with a host round trip.
+ * For every element j < n of every shard, in one fused kernel per shard:
+ *   gs   = sum over k = 0..n_d-1, in that order, of fp32(grads[k][j])
+ *   g    = gs * (float)(1 / (n_d * loss_scale))
+ *   m'   = b1 m + (1 - b1) g;   v' = b2 v + (1 - b2) g^2
+ *   u    = (m' / (1 - beta1^step)) / (sqrt(v' / (1 - beta2^step)) + eps)
+ *   th'  = th - lr (u + weight_decay th);   params[j] = fp16_rn(th')
+ * reading state set `cur`, writing set `cur ^ 1`; every fp32 operation is one
+ * IEEE round-to-nearest step, no fused multiply-add.
+ * The non-finite test of gs over all shards is ORed into *flag_dev (DEVICE
+ * int32 scratch, cleared by this call).  The call then waits for the stream;
+ * on overflow it rewrites every shard's params from master[cur] so the fp16
+ * slice again matches the committed state.  *overflow_out (HOST) gets 0 or 1.
+ * The caller commits: overflow == 0 -> cur ^= 1, step + 1 for the next call;
+ * overflow == 1 -> keep cur and step, halve the loss scale (floor 1).
+ * step >= 1 is the Adam time t of this update (committed updates + 1). */
+ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                               const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
+                               int32_t* flag_dev, void* stream, int32_t* overflow_out);
+
+/* Set up a device control block: loss scale L, t = 0, cur = 0, counters 0.
+ * Stream-ordered (one tiny kernel). */
+ZS_API int32_t zero_ctrl_init(zs_ctrl* ctrl_dev, double loss_scale, void* stream);
+
+/* The same step with no host synchronisation (CUDA-graph friendly): the loss
+ * scale, t and the ping-pong set come from *ctrl_dev, and the commit-or-skip
+ * decision runs on the device.  Enqueues one fused kernel per shard with
+ * n > 0 (zero_shard_reduce_adam_async) and then one commit kernel
+ * (zero_step_commit_async). */
+ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                     const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream);
+
+/* First half of zero_shard_step_async for one shard: the fused reduce +
+ * non-finite test + Adam + fp16 cast kernel, with t = ctrl->step + 1, the
+ * loss scale ctrl->loss_scale and set ctrl->cur; ORs its test into
+ * ctrl->overflow.  Several shards of one step each get one call, then one
+ * zero_step_commit_async for all of them. */
+ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
+                                            zs_ctrl* ctrl_dev, void* stream);
+
+/* Second half: if ctrl->overflow is set, rewrite every listed shard's params
+ * from master[ctrl->cur] and halve the loss scale (floor 1), counting a skip;
+ * otherwise flip ctrl->cur, advance t and beta^t.  Records last_overflow and
+ * clears overflow for the next step.  The shard list must be the shards the
+ * step updated (grads are not used). */
+ZS_API int32_t zero_step_commit_async(const zs_shard* shards, int32_t n_shards, const zs_adam* hp,
+                                      zs_ctrl* ctrl_dev, void* stream);
+
+/* params[j] = fp16_rn(master[j]) for j < n (DEVICE buffers): initialises the
+ * fp16 parameter slice from fp32 master weights.  Stream-ordered. */
+ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params_dev, int64_t n,
+                                       void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics.                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Static description of a status code. */
+ZS_API const char* zero_status_string(int32_t status);
+/* Text of the last ZS_ERR_CUDA failure on the calling host thread ("" if none). */
+ZS_API const char* zero_last_error(void);
+/* Number of kernels this library has enqueued in this process. */
+ZS_API int64_t zero_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_SHARD_H_ */

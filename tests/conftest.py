@@ -17,3 +17,21 @@ def oracle():
     import oracle as _oracle
     _oracle.build()
     return _oracle
+
+
+@pytest.fixture(scope="session")
+def zs():
+    """The product binding with its CUDA library built (nvcc cross-compiles
+    without a GPU; loading the library needs no device)."""
+    from zero_partitioned_mixed_partition_gb300 import binding, build
+    build.build()
+    binding.lib()
+    return binding
+
+
+@pytest.fixture(scope="session")
+def cuda_device():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    return torch.device("cuda", 0)

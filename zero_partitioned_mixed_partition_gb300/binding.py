@@ -1,0 +1,288 @@
+"""ctypes binding of ``libzeroshard.so`` (C ABI in ``include/zero_shard.h``).
+
+Argument marshalling only: every function has the name of the C entry point it
+wraps, turns torch tensors into device pointers and Python values into C
+structs, and raises :class:`ZeroShardError` on a non-zero status.  Every step
+of the computation runs in the library's CUDA kernels.  There is no fallback:
+if the library has not been built, :func:`lib` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Iterable, List, Optional, Sequence
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libzeroshard.so")
+
+ZS_OK, ZS_ERR_ARG, ZS_ERR_ALIGN, ZS_ERR_CUDA, ZS_ERR_TIMEOUT = 0, -1, -2, -3, -4
+ZS_MAX_ND = 1024
+ZS_MAX_SHARDS = 256
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F64 = ctypes.c_double
+
+
+class ZeroShardError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" + (f": {detail}" if detail else ""))
+
+
+class Fragment(ctypes.Structure):
+    _fields_ = [("tensor", _I32), ("shard", _I32), ("tensor_offset", _I64),
+                ("shard_offset", _I64), ("length", _I64)]
+
+
+class Adam(ctypes.Structure):
+    _fields_ = [("lr", _F64), ("beta1", _F64), ("beta2", _F64), ("eps", _F64), ("weight_decay", _F64)]
+
+
+class Shard(ctypes.Structure):
+    _fields_ = [("grads", ctypes.POINTER(_P)), ("master", _P * 2), ("m", _P * 2), ("v", _P * 2),
+                ("params", _P), ("n", _I64)]
+
+
+class Ctrl(ctypes.Structure):
+    _fields_ = [("loss_scale", _F64), ("beta1_pow", _F64), ("beta2_pow", _F64), ("step", _I64),
+                ("skipped", _I64), ("cur", _I32), ("overflow", _I32), ("last_overflow", _I32),
+                ("arrivals", ctypes.c_uint32)]
+
+
+FRAGMENT_DTYPE = np.dtype([("tensor", np.int32), ("shard", np.int32), ("tensor_offset", np.int64),
+                           ("shard_offset", np.int64), ("length", np.int64)])
+assert FRAGMENT_DTYPE.itemsize == ctypes.sizeof(Fragment) == 32
+CTRL_BYTES = ctypes.sizeof(Ctrl)
+
+_lock = threading.Lock()
+_lib = None
+
+_SIGNATURES = {
+    "zero_partition_layout": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P]),
+    "zero_partition_layout_device": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P]),
+    "zero_state_bytes": (_F64, [_F64, _I32, _I32, _F64]),
+    "zero_shard_step": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _P, _P, _P]),
+    "zero_ctrl_init": (_I32, [_P, _F64, _P]),
+    "zero_shard_step_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
+    "zero_shard_reduce_adam_async": (_I32, [_P, _I32, _P, _P, _P]),
+    "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
+    "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
+    "zero_status_string": (ctypes.c_char_p, [_I32]),
+    "zero_last_error": (ctypes.c_char_p, []),
+    "zero_kernel_launches": (_I64, []),
+}
+EXPORTED = tuple(_SIGNATURES)
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                   "(there is no CPU fallback)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    if _lib is None and not os.path.exists(LIB_PATH):
+        return str(status)
+    return lib().zero_status_string(int(status)).decode()
+
+
+def zero_last_error() -> str:
+    return lib().zero_last_error().decode()
+
+
+def zero_kernel_launches() -> int:
+    return int(lib().zero_kernel_launches())
+
+
+def _check(rc: int, what: str):
+    if rc != ZS_OK:
+        raise ZeroShardError(rc, what, zero_last_error() if rc == ZS_ERR_CUDA else "")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev_ptr(t: Optional[torch.Tensor], dtype, what: str) -> Optional[int]:
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{what}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise TypeError(f"{what}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+# ------------------------------------------------------------------ layout ---
+
+def zero_partition_layout(numels: Sequence[int], n_d: int, align: int) -> dict:
+    """Host partition; returns psi, psi_pad, shard_numel, tensor_offsets,
+    shard_offsets (numpy int64) and fragments (numpy structured array)."""
+    L = lib()
+    arr = np.ascontiguousarray(np.asarray(numels, dtype=np.int64))
+    t = arr.size
+    psi, psi_pad, s, nf = _I64(), _I64(), _I64(), _I64()
+    toff = np.empty(t, np.int64)
+    soff = np.empty(max(int(n_d), 0) + 1, np.int64)
+    rc = L.zero_partition_layout(arr.ctypes.data if t else None, t, int(n_d), int(align),
+                                 ctypes.byref(psi), ctypes.byref(psi_pad), ctypes.byref(s),
+                                 toff.ctypes.data if t else None, soff.ctypes.data, None, 0,
+                                 ctypes.byref(nf))
+    _check(rc, "zero_partition_layout")
+    frags = np.zeros(nf.value, FRAGMENT_DTYPE)
+    rc = L.zero_partition_layout(arr.ctypes.data if t else None, t, int(n_d), int(align),
+                                 ctypes.byref(psi), ctypes.byref(psi_pad), ctypes.byref(s),
+                                 toff.ctypes.data if t else None, soff.ctypes.data,
+                                 frags.ctypes.data if nf.value else None, nf.value, ctypes.byref(nf))
+    _check(rc, "zero_partition_layout")
+    return {"psi": psi.value, "psi_pad": psi_pad.value, "shard_numel": s.value,
+            "tensor_offsets": toff, "shard_offsets": soff, "fragments": frags}
+
+
+def zero_partition_layout_device(numels_dev: torch.Tensor, n_d: int, align: int, scalars_dev: torch.Tensor,
+                                 tensor_offsets_dev: torch.Tensor, shard_offsets_dev: torch.Tensor,
+                                 frags_dev: Optional[torch.Tensor], frag_cap: int, stream=None):
+    """Device partition (stream-ordered).  ``frags_dev`` is a byte or int64
+    tensor of at least 32 * frag_cap bytes, or None."""
+    fptr = None
+    if frags_dev is not None:
+        if frags_dev.numel() * frags_dev.element_size() < 32 * frag_cap:
+            raise ValueError("frags_dev too small for frag_cap")
+        fptr = _dev_ptr(frags_dev, frags_dev.dtype, "frags_dev")
+    n = numels_dev.numel()
+    rc = lib().zero_partition_layout_device(
+        _dev_ptr(numels_dev, torch.int64, "numels_dev") if n else None, n, int(n_d), int(align),
+        _dev_ptr(scalars_dev, torch.int64, "scalars_dev"),
+        _dev_ptr(tensor_offsets_dev, torch.int64, "tensor_offsets_dev") if n else None,
+        _dev_ptr(shard_offsets_dev, torch.int64, "shard_offsets_dev"), fptr, int(frag_cap), _stream(stream))
+    _check(rc, "zero_partition_layout_device")
+
+
+def fragments_from_bytes(raw: np.ndarray, count: int) -> np.ndarray:
+    """View a host copy of a device fragment table as the structured dtype."""
+    return np.frombuffer(np.ascontiguousarray(raw).tobytes(), dtype=FRAGMENT_DTYPE, count=count)
+
+
+def zero_state_bytes(psi: float, n_d: int, stage: int, k: float = 12.0) -> float:
+    return float(lib().zero_state_bytes(float(psi), int(n_d), int(stage), float(k)))
+
+
+# ------------------------------------------------------------------ shards ---
+
+class ShardView:
+    """One shard's device buffers, and the C struct that describes them.
+
+    grads: list of n_d fp16 CUDA tensors (each >= n elements);
+    master, m, v: pairs (set 0, set 1) of fp32 CUDA tensors (the same tensor
+    twice means in-place); params: fp16 CUDA tensor (the shard's slice of the
+    full parameter buffer); n: elements stepped."""
+
+    def __init__(self, grads: Sequence[torch.Tensor], master, m, v, params: torch.Tensor, n: int):
+        self.grads = list(grads)
+        self.master, self.m, self.v = tuple(master), tuple(m), tuple(v)
+        self.params = params
+        self.n = int(n)
+        self._table = (_P * max(len(self.grads), 1))(
+            *[_dev_ptr(g, torch.float16, "grads") for g in self.grads])
+        self.struct = Shard()
+        self.struct.grads = ctypes.cast(self._table, ctypes.POINTER(_P))
+        for i in range(2):
+            self.struct.master[i] = _dev_ptr(self.master[i], torch.float32, "master")
+            self.struct.m[i] = _dev_ptr(self.m[i], torch.float32, "m")
+            self.struct.v[i] = _dev_ptr(self.v[i], torch.float32, "v")
+        self.struct.params = _dev_ptr(params, torch.float16, "params")
+        self.struct.n = self.n
+
+    @property
+    def n_d(self) -> int:
+        return len(self.grads)
+
+
+def _shard_array(shards: Sequence[ShardView]):
+    arr = (Shard * len(shards))()
+    for i, s in enumerate(shards):
+        arr[i] = s.struct
+    return arr
+
+
+def adam(lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+         weight_decay: float = 0.0) -> Adam:
+    return Adam(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay))
+
+
+def zero_shard_step(shards: Sequence[ShardView], n_d: int, hp: Adam, loss_scale: float, step: int, cur: int,
+                    flag_dev: torch.Tensor, stream=None) -> int:
+    """Synchronous step over ``shards``; returns the overflow flag (0/1)."""
+    arr = _shard_array(shards)
+    ovf = _I32(-1)
+    rc = lib().zero_shard_step(arr, len(shards), int(n_d), ctypes.byref(hp), float(loss_scale), int(step),
+                               int(cur), _dev_ptr(flag_dev, torch.int32, "flag_dev"), _stream(stream),
+                               ctypes.byref(ovf))
+    _check(rc, "zero_shard_step")
+    return int(ovf.value)
+
+
+def new_ctrl(device="cuda") -> torch.Tensor:
+    """Device memory for one zs_ctrl (int64-typed so it is 8-byte aligned)."""
+    return torch.zeros((CTRL_BYTES + 7) // 8, dtype=torch.int64, device=device)
+
+
+def zero_ctrl_init(ctrl_dev: torch.Tensor, loss_scale: float, stream=None):
+    rc = lib().zero_ctrl_init(_dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), float(loss_scale), _stream(stream))
+    _check(rc, "zero_ctrl_init")
+
+
+def zero_shard_step_async(shards: Sequence[ShardView], n_d: int, hp: Adam, ctrl_dev: torch.Tensor, stream=None):
+    arr = _shard_array(shards)
+    rc = lib().zero_shard_step_async(arr, len(shards), int(n_d), ctypes.byref(hp),
+                                     _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_step_async")
+
+
+def zero_shard_reduce_adam_async(shard: ShardView, n_d: int, hp: Adam, ctrl_dev: torch.Tensor, stream=None):
+    rc = lib().zero_shard_reduce_adam_async(ctypes.byref(shard.struct), int(n_d), ctypes.byref(hp),
+                                            _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_reduce_adam_async")
+
+
+def zero_step_commit_async(shards: Sequence[ShardView], hp: Adam, ctrl_dev: torch.Tensor, stream=None):
+    arr = _shard_array(shards)
+    rc = lib().zero_step_commit_async(arr, len(shards), ctypes.byref(hp),
+                                      _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_step_commit_async")
+
+
+def zero_params_from_master(master: torch.Tensor, params: torch.Tensor, n: int, stream=None):
+    rc = lib().zero_params_from_master(_dev_ptr(master, torch.float32, "master"),
+                                       _dev_ptr(params, torch.float16, "params"), int(n), _stream(stream))
+    _check(rc, "zero_params_from_master")
+
+
+def read_ctrl(ctrl_dev: torch.Tensor) -> dict:
+    """Host snapshot of a device control block (synchronises the copy)."""
+    raw = ctrl_dev.detach().cpu().numpy().tobytes()[:CTRL_BYTES]
+    c = Ctrl.from_buffer_copy(raw)
+    return {name: getattr(c, name) for name, _ in Ctrl._fields_}

@@ -1,0 +1,586 @@
+// shard_step.cu -- the fused ZeRO shard step for sm_103a and its C ABI.
+//
+// One rank's optimizer step over its shard ("ZeRO Stage 1 Math", "The
+// per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec. 2.1 Fact 1):
+//   reduce   gs_j = sum_k fp32(h_k[j]) over the N_d fp16 contributions, in
+//            rank order, g_j = gs_j * (float)(1 / (N_d L))      (averaged,
+//            and the loss scale L removed)
+//   test     any non-finite gs_j in the valid range -> overflow for the step
+//   Adam     m' = b1 m + (1-b1) g,  v' = b2 v + (1-b2) g^2,
+//            u = (m'/(1-b1^t)) / (sqrt(v'/(1-b2^t)) + eps),
+//            th' = th - lr (u + wd th)                 (wd = 0: plain Adam)
+//   cast     params_j = fp16_rn(th')
+// all in one pass over memory.  The step is elementwise with O(1) work per
+// parameter and touches every byte once, so it is bound by HBM bandwidth: per
+// stepped element it reads 2 N_d + 12 bytes and writes 12 + 2 bytes.  The
+// kernel therefore streams 16-byte vectors (8 parameters per thread and
+// iteration) with evict-first cache hints, runs a persistent grid sized from
+// the SM count and occupancy, and keeps every fp32 operation a single IEEE
+// round-to-nearest step (explicit _rn intrinsics, no fused multiply-add), so
+// its results are reproducible bit for bit.
+//
+// Skip without a second pass: the non-finite test is only known once the whole
+// step has run, so the state is double-buffered.  A step reads set `cur` and
+// writes set `cur ^ 1`; committing flips `cur`, skipping leaves it and only the
+// fp16 slice (already overwritten) is re-cast from the kept master weights.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "zs_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;          // threads per block of the fused kernel
+constexpr int kCommitThreads = 512;    // threads per block of the commit kernel
+constexpr int kCastThreads = 256;
+
+// ------------------------------------------------------------ coefficients ---
+
+// Scalar coefficients of one step, each formed in double and rounded once to
+// float, so host and device agree bit for bit.
+struct Coef {
+    float b1, c1, b2, c2;  // beta1, 1 - beta1, beta2, 1 - beta2
+    float bc1, bc2;        // 1 - beta1^t, 1 - beta2^t
+    float lr, eps, wd;
+    float inv;             // 1 / (N_d L)
+};
+
+Coef coef_host(const zs_adam& hp, double p1, double p2, int n_d, double loss_scale) {
+    Coef c;
+    c.b1 = (float)hp.beta1;
+    c.c1 = (float)(1.0 - hp.beta1);
+    c.b2 = (float)hp.beta2;
+    c.c2 = (float)(1.0 - hp.beta2);
+    c.bc1 = (float)(1.0 - p1);
+    c.bc2 = (float)(1.0 - p2);
+    c.lr = (float)hp.lr;
+    c.eps = (float)hp.eps;
+    c.wd = (float)hp.weight_decay;
+    c.inv = (float)(1.0 / ((double)n_d * loss_scale));
+    return c;
+}
+
+__device__ Coef coef_device(const zs_adam& hp, double p1, double p2, int n_d, double loss_scale) {
+    Coef c;
+    c.b1 = __double2float_rn(hp.beta1);
+    c.c1 = __double2float_rn(__dsub_rn(1.0, hp.beta1));
+    c.b2 = __double2float_rn(hp.beta2);
+    c.c2 = __double2float_rn(__dsub_rn(1.0, hp.beta2));
+    c.bc1 = __double2float_rn(__dsub_rn(1.0, p1));
+    c.bc2 = __double2float_rn(__dsub_rn(1.0, p2));
+    c.lr = __double2float_rn(hp.lr);
+    c.eps = __double2float_rn(hp.eps);
+    c.wd = __double2float_rn(hp.weight_decay);
+    c.inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)n_d, loss_scale)));
+    return c;
+}
+
+// ------------------------------------------------------------ element math ---
+
+__device__ __forceinline__ bool nonfinite(float x) {
+    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
+}
+
+// One Adam / AdamW update of one coordinate from its summed gradient gs.
+__device__ __forceinline__ void adam_update(const Coef& c, float gs, float& th, float& m, float& v) {
+    const float g = __fmul_rn(gs, c.inv);
+    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.c1, g));
+    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.c2, __fmul_rn(g, g)));
+    const float mh = __fdiv_rn(m, c.bc1);
+    const float vh = __fdiv_rn(v, c.bc2);
+    const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), c.eps));
+    th = __fsub_rn(th, __fmul_rn(c.lr, __fadd_rn(u, __fmul_rn(c.wd, th))));
+}
+
+// --------------------------------------------------------- vector memory ---
+
+// VEC elements per access: 8 (16-byte fp16 / 2 x 16-byte fp32 streaming
+// accesses) or 1 (scalar, any naturally aligned pointer).
+template <int VEC> struct Mem;
+
+template <> struct Mem<8> {
+    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
+        const uint4 r = __ldcs(reinterpret_cast<const uint4*>(p));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void load_f(const float* p, float* out) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(p + 4));
+        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    }
+    static __device__ __forceinline__ void store_f(float* p, const float* in) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(in[0], in[1], in[2], in[3]));
+        __stcs(reinterpret_cast<float4*>(p + 4), make_float4(in[4], in[5], in[6], in[7]));
+    }
+    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        __stcs(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
+    }
+};
+
+template <> struct Mem<1> {
+    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
+        out[0] = __half2float(__ushort_as_half(__ldcs(reinterpret_cast<const unsigned short*>(p))));
+    }
+    static __device__ __forceinline__ void load_f(const float* p, float* out) { out[0] = __ldcs(p); }
+    static __device__ __forceinline__ void store_f(float* p, const float* in) { __stcs(p, in[0]); }
+    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
+        __stcs(reinterpret_cast<unsigned short*>(p), __half_as_ushort(__float2half_rn(in[0])));
+    }
+};
+
+// ------------------------------------------------------------ fused kernel ---
+
+// Kernel parameters (passed by value, so the contribution table needs no
+// device memory).  CAP bounds n_d and sizes the pointer table.
+template <int CAP>
+struct StepArgs {
+    const uint16_t* grads[CAP];
+    float* master[2];
+    float* m[2];
+    float* v[2];
+    uint16_t* params;
+    int64_t n;
+    int32_t n_d;
+    int32_t cur;          // host-resolved ping-pong set (ctrl == nullptr)
+    Coef coef;            // host-resolved coefficients (ctrl == nullptr)
+    zs_adam hp;           // hyper-parameters for device-resolved coefficients
+    const zs_ctrl* ctrl;  // non-null: loss scale, t and cur come from here
+    int32_t* flag;        // overflow accumulator (ORed)
+};
+
+// VEC elements of the shard starting at element e: reduce, test, update, cast.
+template <int CAP, int VEC>
+__device__ __forceinline__ uint32_t step_elements(const StepArgs<CAP>& p, const Coef& c, int64_t e,
+                                                  const float* th_in, const float* m_in,
+                                                  const float* v_in, float* th_out, float* m_out,
+                                                  float* v_out) {
+    float th[VEC], m[VEC], v[VEC], acc[VEC];
+    Mem<VEC>::load_f(th_in + e, th);
+    Mem<VEC>::load_f(m_in + e, m);
+    Mem<VEC>::load_f(v_in + e, v);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
+#pragma unroll 4
+    for (int k = 0; k < p.n_d; ++k) {
+        float h[VEC];
+        Mem<VEC>::load_h(p.grads[k] + e, h);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[j] = __fadd_rn(acc[j], h[j]);
+    }
+    uint32_t bad = 0;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        bad |= nonfinite(acc[j]) ? 1u : 0u;
+        adam_update(c, acc[j], th[j], m[j], v[j]);
+    }
+    Mem<VEC>::store_f(th_out + e, th);
+    Mem<VEC>::store_f(m_out + e, m);
+    Mem<VEC>::store_f(v_out + e, v);
+    Mem<VEC>::store_h(p.params + e, th);
+    return bad;
+}
+
+template <int CAP, int VEC>
+__global__ void __launch_bounds__(kThreads) shard_step_kernel(const __grid_constant__ StepArgs<CAP> p) {
+    __shared__ Coef s_coef;
+    __shared__ int s_cur;
+    if (threadIdx.x == 0) {
+        if (p.ctrl != nullptr) {
+            const zs_ctrl* ctrl = p.ctrl;
+            const double p1 = __dmul_rn(ctrl->beta1_pow, p.hp.beta1);  // beta1^(t+1)
+            const double p2 = __dmul_rn(ctrl->beta2_pow, p.hp.beta2);
+            s_coef = coef_device(p.hp, p1, p2, p.n_d, ctrl->loss_scale);
+            s_cur = ctrl->cur;
+        } else {
+            s_coef = p.coef;
+            s_cur = p.cur;
+        }
+    }
+    __syncthreads();
+    const Coef c = s_coef;
+    const int cur = s_cur;
+    const float* th_in = p.master[cur];
+    const float* m_in = p.m[cur];
+    const float* v_in = p.v[cur];
+    float* th_out = p.master[cur ^ 1];
+    float* m_out = p.m[cur ^ 1];
+    float* v_out = p.v[cur ^ 1];
+
+    uint32_t bad = 0;
+    const int64_t nvec = p.n / VEC;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
+        bad |= step_elements<CAP, VEC>(p, c, i * VEC, th_in, m_in, v_in, th_out, m_out, v_out);
+    if (VEC > 1) {  // ragged tail: fewer than VEC elements, one per thread of block 0
+        const int64_t e = nvec * VEC + threadIdx.x;
+        if (blockIdx.x == 0 && e < p.n)
+            bad |= step_elements<CAP, 1>(p, c, e, th_in, m_in, v_in, th_out, m_out, v_out);
+    }
+    // overflow: warp/block OR, one atomic per block that saw a non-finite value
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
+}
+
+// ---------------------------------------------------------- commit kernel ---
+
+struct CommitShard {
+    uint16_t* params;
+    const float* master[2];
+    int64_t n;
+};
+
+template <int MAXS>
+struct CommitArgs {
+    CommitShard shards[MAXS];
+    int32_t n_shards;
+    double beta1, beta2;
+    zs_ctrl* ctrl;
+};
+
+// params = fp16_rn(master) over [0, n) by the whole grid.
+__device__ __forceinline__ void cast_range(const float* master, uint16_t* params, int64_t n, int64_t tid,
+                                           int64_t stride) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(master) | reinterpret_cast<uintptr_t>(params)) & 15) == 0;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nvec = n / 8;
+        for (int64_t i = tid; i < nvec; i += stride) {
+            float x[8];
+            Mem<8>::load_f(master + 8 * i, x);
+            Mem<8>::store_h(params + 8 * i, x);
+        }
+        done = nvec * 8;
+    }
+    for (int64_t j = done + tid; j < n; j += stride) {
+        float x[1];
+        Mem<1>::load_f(master + j, x);
+        Mem<1>::store_h(params + j, x);
+    }
+}
+
+// End of a step on the device: restore the fp16 slices if the step overflowed,
+// then the last block to finish commits or skips in the control block.
+template <int MAXS>
+__global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ CommitArgs<MAXS> p) {
+    __shared__ int s_ovf, s_cur;
+    zs_ctrl* ctrl = p.ctrl;
+    if (threadIdx.x == 0) {
+        s_ovf = *reinterpret_cast<volatile int32_t*>(&ctrl->overflow);
+        s_cur = *reinterpret_cast<volatile int32_t*>(&ctrl->cur);
+    }
+    __syncthreads();
+    if (s_ovf) {
+        const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+        for (int s = 0; s < p.n_shards; ++s)
+            cast_range(p.shards[s].master[s_cur], p.shards[s].params, p.shards[s].n, tid, stride);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&ctrl->arrivals, 1u);
+        if (prev == gridDim.x - 1) {
+            // every block has read overflow and cur: finish the step
+            __threadfence();
+            volatile zs_ctrl* c = ctrl;
+            const int ovf = c->overflow;
+            c->last_overflow = ovf;
+            if (ovf) {
+                const double half = __dmul_rn(c->loss_scale, 0.5);
+                c->loss_scale = half < 1.0 ? 1.0 : half;
+                c->skipped = c->skipped + 1;
+            } else {
+                c->cur = c->cur ^ 1;
+                c->step = c->step + 1;
+                c->beta1_pow = __dmul_rn(c->beta1_pow, p.beta1);
+                c->beta2_pow = __dmul_rn(c->beta2_pow, p.beta2);
+            }
+            c->overflow = 0;
+            c->arrivals = 0u;
+            __threadfence();
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kCastThreads) cast_kernel(const float* master, uint16_t* params, int64_t n) {
+    cast_range(master, params, n, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+}
+
+__global__ void ctrl_init_kernel(zs_ctrl* ctrl, double loss_scale) {
+    zs_ctrl c;
+    c.loss_scale = loss_scale;
+    c.beta1_pow = 1.0;
+    c.beta2_pow = 1.0;
+    c.step = 0;
+    c.skipped = 0;
+    c.cur = 0;
+    c.overflow = 0;
+    c.last_overflow = 0;
+    c.arrivals = 0u;
+    *ctrl = c;
+}
+
+// ------------------------------------------------------------ host helpers ---
+
+// Persistent grid: enough blocks to fill every SM at the kernel's occupancy,
+// never more than the work needs.
+int persistent_blocks(const void* kernel, int threads, int64_t work_items) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> per_sm;
+    int bps = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = per_sm.find(kernel);
+        if (it != per_sm.end()) bps = it->second;
+    }
+    if (bps == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, threads, 0) != cudaSuccess || bps < 1)
+            bps = 1;
+        std::lock_guard<std::mutex> lock(mu);
+        per_sm[kernel] = bps;
+    }
+    const int64_t full = (int64_t)bps * zs::device_sm_count();
+    const int64_t need = (work_items + threads - 1) / threads;
+    int64_t blocks = need < full ? need : full;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+bool valid_hp(const zs_adam* hp) {
+    if (hp == nullptr) return false;
+    const double v[] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+    for (double x : v)
+        if (!(x == x) || x > 1e300 || x < -1e300) return false;
+    return hp->beta1 >= 0.0 && hp->beta1 < 1.0 && hp->beta2 >= 0.0 && hp->beta2 < 1.0 && hp->eps >= 0.0;
+}
+
+// Checks one shard; *vec is set when every pointer allows 16-byte accesses.
+int32_t check_shard(const zs_shard& s, int32_t n_d, bool* vec) {
+    if (s.n < 0) return ZS_ERR_ARG;
+    *vec = true;
+    if (s.n == 0) return ZS_OK;
+    if (s.grads == nullptr || s.params == nullptr) return ZS_ERR_ARG;
+    for (int i = 0; i < 2; ++i)
+        if (!s.master[i] || !s.m[i] || !s.v[i]) return ZS_ERR_ARG;
+    for (int k = 0; k < n_d; ++k) {
+        if (s.grads[k] == nullptr) return ZS_ERR_ARG;
+        if (!zs::aligned_to(s.grads[k], 2)) return ZS_ERR_ALIGN;
+        if (!zs::aligned_to(s.grads[k], 16)) *vec = false;
+    }
+    if (!zs::aligned_to(s.params, 2)) return ZS_ERR_ALIGN;
+    if (!zs::aligned_to(s.params, 16)) *vec = false;
+    for (int i = 0; i < 2; ++i) {
+        const void* st[] = {s.master[i], s.m[i], s.v[i]};
+        for (const void* q : st) {
+            if (!zs::aligned_to(q, 4)) return ZS_ERR_ALIGN;
+            if (!zs::aligned_to(q, 16)) *vec = false;
+        }
+    }
+    return ZS_OK;
+}
+
+template <int CAP>
+int32_t launch_step_cap(const zs_shard& s, int32_t n_d, bool vec, const Coef* coef, int32_t cur,
+                        const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
+    StepArgs<CAP> a;
+    for (int k = 0; k < CAP; ++k) a.grads[k] = k < n_d ? s.grads[k] : nullptr;
+    for (int i = 0; i < 2; ++i) {
+        a.master[i] = s.master[i];
+        a.m[i] = s.m[i];
+        a.v[i] = s.v[i];
+    }
+    a.params = s.params;
+    a.n = s.n;
+    a.n_d = n_d;
+    a.cur = cur;
+    if (coef) a.coef = *coef; else a.coef = Coef{};
+    a.hp = hp;
+    a.ctrl = ctrl;
+    a.flag = flag;
+    if (vec) {
+        const void* k = (const void*)shard_step_kernel<CAP, 8>;
+        const int blocks = persistent_blocks(k, kThreads, s.n / 8 > 0 ? s.n / 8 : 1);
+        shard_step_kernel<CAP, 8><<<blocks, kThreads, 0, stream>>>(a);
+    } else {
+        const void* k = (const void*)shard_step_kernel<CAP, 1>;
+        const int blocks = persistent_blocks(k, kThreads, s.n);
+        shard_step_kernel<CAP, 1><<<blocks, kThreads, 0, stream>>>(a);
+    }
+    return zs::check_launch("shard_step_kernel");
+}
+
+int32_t launch_step(const zs_shard& s, int32_t n_d, bool vec, const Coef* coef, int32_t cur,
+                    const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
+    if (n_d <= 4) return launch_step_cap<4>(s, n_d, vec, coef, cur, hp, ctrl, flag, stream);
+    if (n_d <= 16) return launch_step_cap<16>(s, n_d, vec, coef, cur, hp, ctrl, flag, stream);
+    if (n_d <= 64) return launch_step_cap<64>(s, n_d, vec, coef, cur, hp, ctrl, flag, stream);
+    return launch_step_cap<ZS_MAX_ND>(s, n_d, vec, coef, cur, hp, ctrl, flag, stream);
+}
+
+int32_t launch_cast(const float* master, uint16_t* params, int64_t n, cudaStream_t stream) {
+    if (n == 0) return ZS_OK;
+    const int blocks = persistent_blocks((const void*)cast_kernel, kCastThreads, (n + 7) / 8);
+    cast_kernel<<<blocks, kCastThreads, 0, stream>>>(master, params, n);
+    return zs::check_launch("cast_kernel");
+}
+
+template <int MAXS>
+int32_t launch_commit_cap(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
+                          cudaStream_t stream) {
+    CommitArgs<MAXS> a;
+    for (int i = 0; i < MAXS; ++i) {
+        if (i < n_shards) {
+            a.shards[i].params = shards[i].params;
+            a.shards[i].master[0] = shards[i].master[0];
+            a.shards[i].master[1] = shards[i].master[1];
+            a.shards[i].n = shards[i].n;
+        } else {
+            a.shards[i] = CommitShard{nullptr, {nullptr, nullptr}, 0};
+        }
+    }
+    a.n_shards = n_shards;
+    a.beta1 = hp.beta1;
+    a.beta2 = hp.beta2;
+    a.ctrl = ctrl;
+    // one block per SM: enough to restore the slices at full bandwidth on an
+    // overflow step, few enough that a normal step costs only the arrivals
+    const int blocks = zs::device_sm_count();
+    commit_kernel<MAXS><<<blocks, kCommitThreads, 0, stream>>>(a);
+    return zs::check_launch("commit_kernel");
+}
+
+int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
+                      cudaStream_t stream) {
+    if (n_shards <= 1) return launch_commit_cap<1>(shards, n_shards, hp, ctrl, stream);
+    if (n_shards <= 16) return launch_commit_cap<16>(shards, n_shards, hp, ctrl, stream);
+    return launch_commit_cap<ZS_MAX_SHARDS>(shards, n_shards, hp, ctrl, stream);
+}
+
+int32_t check_shard_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, bool* vec) {
+    if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS) return ZS_ERR_ARG;
+    for (int32_t i = 0; i < n_shards; ++i) {
+        int32_t rc = check_shard(shards[i], n_d, &vec[i]);
+        if (rc != ZS_OK) return rc;
+    }
+    return ZS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                               const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
+                               int32_t* flag_dev, void* stream, int32_t* overflow_out) {
+    if (n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || !(loss_scale > 0.0) || loss_scale > 1e300 ||
+        step < 1 || (cur != 0 && cur != 1) || flag_dev == nullptr || overflow_out == nullptr)
+        return ZS_ERR_ARG;
+    if (!zs::aligned_to(flag_dev, 4)) return ZS_ERR_ALIGN;
+    bool vec[ZS_MAX_SHARDS];
+    int32_t rc = check_shard_list(shards, n_shards, n_d, vec);
+    if (rc != ZS_OK) return rc;
+
+    // Adam time t = step: beta^t by repeated multiplication
+    double p1 = 1.0, p2 = 1.0;
+    for (int64_t i = 0; i < step; ++i) {
+        p1 *= hp->beta1;
+        p2 *= hp->beta2;
+    }
+    const Coef coef = coef_host(*hp, p1, p2, n_d, loss_scale);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t err = cudaMemsetAsync(flag_dev, 0, sizeof(int32_t), st);
+    if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step: clear flag");
+    for (int32_t i = 0; i < n_shards; ++i) {
+        if (shards[i].n == 0) continue;
+        rc = launch_step(shards[i], n_d, vec[i], &coef, cur, *hp, nullptr, flag_dev, st);
+        if (rc != ZS_OK) return rc;
+    }
+    int32_t flag = 0;
+    err = cudaMemcpyAsync(&flag, flag_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step: read flag");
+    if (flag) {
+        for (int32_t i = 0; i < n_shards; ++i) {
+            rc = launch_cast(shards[i].master[cur], shards[i].params, shards[i].n, st);
+            if (rc != ZS_OK) return rc;
+        }
+        err = cudaStreamSynchronize(st);
+        if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step: restore");
+    }
+    *overflow_out = flag ? 1 : 0;
+    return ZS_OK;
+}
+
+ZS_API int32_t zero_ctrl_init(zs_ctrl* ctrl_dev, double loss_scale, void* stream) {
+    if (ctrl_dev == nullptr || !(loss_scale > 0.0) || loss_scale > 1e300) return ZS_ERR_ARG;
+    if (!zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
+    ctrl_init_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(ctrl_dev, loss_scale);
+    return zs::check_launch("zero_ctrl_init");
+}
+
+ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
+                                            zs_ctrl* ctrl_dev, void* stream) {
+    if (shard == nullptr || n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || ctrl_dev == nullptr)
+        return ZS_ERR_ARG;
+    if (!zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
+    bool vec = true;
+    int32_t rc = check_shard(*shard, n_d, &vec);
+    if (rc != ZS_OK) return rc;
+    if (shard->n == 0) return ZS_OK;
+    return launch_step(*shard, n_d, vec, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow,
+                       (cudaStream_t)stream);
+}
+
+ZS_API int32_t zero_step_commit_async(const zs_shard* shards, int32_t n_shards, const zs_adam* hp,
+                                      zs_ctrl* ctrl_dev, void* stream) {
+    if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS || !valid_hp(hp) || ctrl_dev == nullptr)
+        return ZS_ERR_ARG;
+    if (!zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
+    for (int32_t i = 0; i < n_shards; ++i) {
+        const zs_shard& s = shards[i];
+        if (s.n < 0) return ZS_ERR_ARG;
+        if (s.n > 0 && (!s.params || !s.master[0] || !s.master[1])) return ZS_ERR_ARG;
+        if (!zs::aligned_to(s.params, 2) || !zs::aligned_to(s.master[0], 4) || !zs::aligned_to(s.master[1], 4))
+            return ZS_ERR_ALIGN;
+    }
+    return launch_commit(shards, n_shards, *hp, ctrl_dev, (cudaStream_t)stream);
+}
+
+ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                     const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream) {
+    if (n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || ctrl_dev == nullptr) return ZS_ERR_ARG;
+    if (!zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
+    bool vec[ZS_MAX_SHARDS];
+    int32_t rc = check_shard_list(shards, n_shards, n_d, vec);
+    if (rc != ZS_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int32_t i = 0; i < n_shards; ++i) {
+        if (shards[i].n == 0) continue;
+        rc = launch_step(shards[i], n_d, vec[i], nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, st);
+        if (rc != ZS_OK) return rc;
+    }
+    return launch_commit(shards, n_shards, *hp, ctrl_dev, st);
+}
+
+ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params_dev, int64_t n,
+                                       void* stream) {
+    if (n < 0 || (n > 0 && (master_dev == nullptr || params_dev == nullptr))) return ZS_ERR_ARG;
+    if (!zs::aligned_to(master_dev, 4) || !zs::aligned_to(params_dev, 2)) return ZS_ERR_ALIGN;
+    return launch_cast(master_dev, params_dev, n, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// zs_internal.h -- declarations shared by the translation units of
+// libzeroshard.so (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zero_shard.h"
+
+namespace zs {
+
+// Records a CUDA failure for zero_last_error() and returns ZS_ERR_CUDA.
+int32_t cuda_fail(cudaError_t err, const char* where);
+// Adds n to the count reported by zero_kernel_launches().
+void count_launches(int64_t n);
+
+inline bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks the launch that was just enqueued.
+inline int32_t check_launch(const char* where, int64_t n = 1) {
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return cuda_fail(err, where);
+    count_launches(n);
+    return ZS_OK;
+}
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace zs

@@ -1,0 +1,99 @@
+"""Device buffers for one workload and its steps through the C ABI.
+
+Plumbing only: torch allocates the memory and draws the seeded inputs
+(``synth``); the partition, the fused step and the commit run in the library's
+kernels through :mod:`binding`.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import binding, synth
+
+
+class WorkloadRunner:
+    """Simulates one or more ranks of a workload on one GPU.
+
+    For every stepped shard r it holds the N_d fp16 gradient contributions
+    (one per simulated rank, S elements each, zero past the shard's real
+    parameters), two sets of fp32 master/m/v and the shard's slice of the full
+    fp16 parameter buffer, plus one device control block shared by the shards
+    (they form one step, committed or skipped together)."""
+
+    def __init__(self, w: synth.Workload, device, shards: Optional[Sequence[int]] = None,
+                 with_full_params: bool = True,
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.w = w
+        self.device = torch.device(device)
+        self.stream = stream
+        self.layout = binding.zero_partition_layout(w.numels, w.n_d, w.align)
+        lay = self.layout
+        self.S = int(lay["shard_numel"])
+        if shards is None:
+            shards = [w.rank] if w.rank is not None else list(range(w.n_d))
+        self.shard_ids = list(shards)
+        fr = lay["fragments"]
+        valid = np.bincount(fr["shard"], weights=fr["length"], minlength=w.n_d).astype(np.int64)
+        self.n_valid = {r: int(valid[r]) for r in self.shard_ids}
+        self.hp = binding.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+
+        nshards_full = w.n_d if with_full_params else len(self.shard_ids)
+        self.params_full = torch.zeros(nshards_full * self.S, dtype=torch.float16, device=self.device)
+        self.grads = {}
+        self.state = {}
+        self.views: List[binding.ShardView] = []
+        for i, r in enumerate(self.shard_ids):
+            n = self.n_valid[r]
+            g = [synth.grad_contribution(w, n, k, 1, shard=r, device=self.device, n_alloc=self.S)
+                 for k in range(w.n_d)]
+            master0 = synth.master_init(w, n, shard=r, device=self.device, n_alloc=self.S)
+            master = (master0, torch.zeros_like(master0))
+            m = (torch.zeros_like(master0), torch.zeros_like(master0))
+            v = (torch.zeros_like(master0), torch.zeros_like(master0))
+            slot = r if with_full_params else i
+            params = self.params_full[slot * self.S:(slot + 1) * self.S]
+            self.grads[r] = g
+            self.state[r] = (master, m, v, params)
+            self.views.append(binding.ShardView(g, master, m, v, params, n))
+            binding.zero_params_from_master(master0, params, n, stream=self.stream)
+        self.ctrl = binding.new_ctrl(self.device)
+        binding.zero_ctrl_init(self.ctrl, w.loss_scale, stream=self.stream)
+
+    # ---------------------------------------------------------------- steps --
+    def step(self):
+        """One whole step over every stepped shard, stream-ordered."""
+        binding.zero_shard_step_async(self.views, self.w.n_d, self.hp, self.ctrl, stream=self.stream)
+
+    def reduce_adam(self, i: int = 0):
+        binding.zero_shard_reduce_adam_async(self.views[i], self.w.n_d, self.hp, self.ctrl, stream=self.stream)
+
+    def commit(self):
+        binding.zero_step_commit_async(self.views, self.hp, self.ctrl, stream=self.stream)
+
+    def refresh_grads(self, step: int):
+        """Draw the contributions of ``step`` (workloads with fresh gradients)."""
+        for r in self.shard_ids:
+            n = self.n_valid[r]
+            for k in range(self.w.n_d):
+                self.grads[r][k].copy_(synth.grad_contribution(self.w, n, k, step, shard=r, device=self.device,
+                                                               n_alloc=self.S))
+
+    def ctrl_host(self) -> dict:
+        return binding.read_ctrl(self.ctrl)
+
+    def current(self, r: int):
+        """(master, m, v, params) tensors holding the committed state of shard r."""
+        cur = self.ctrl_host()["cur"]
+        master, m, v, params = self.state[r]
+        return master[cur], m[cur], v[cur], params
+
+    # ------------------------------------------------------------ accounting --
+    def bytes_per_step(self) -> int:
+        """Algorithmic HBM bytes of one step: (26 + 2 N_d) per stepped element."""
+        return sum((26 + 2 * self.w.n_d) * self.n_valid[r] for r in self.shard_ids)
+
+    def elements_per_step(self) -> int:
+        return sum(self.n_valid[r] for r in self.shard_ids)
