@@ -93,9 +93,11 @@ typedef struct zs_adam {
  *             maps to (params_full + rank * shard_numel), >= n values.
  *   n         elements stepped: the shard's real (non-padding) parameters.
  *             Elements past n are not read or written.
- * The vectorised kernel is used when every pointer is 16-byte aligned; any
- * other 4-byte (fp32) / 2-byte (fp16) aligned layout takes a scalar kernel
- * with the same arithmetic. */
+ * Access width follows alignment: with every fp32 buffer 32-byte aligned and
+ * every fp16 buffer 16-byte aligned the kernel moves 16 elements per thread
+ * and iteration (used when n_d > 4); with 16-byte alignment, 8; any other
+ * 4-byte (fp32) / 2-byte (fp16) aligned layout takes a scalar kernel.  All
+ * three do the same arithmetic in the same order. */
 typedef struct zs_shard {
     const uint16_t* const* grads;
     float* master[2];
@@ -229,6 +231,21 @@ ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, 
  * step updated (grads are not used). */
 ZS_API int32_t zero_step_commit_async(const zs_shard* shards, int32_t n_shards, const zs_adam* hp,
                                       zs_ctrl* ctrl_dev, void* stream);
+
+/* The whole step with the gradient contributions and the fp16 shard in HOST
+ * memory, for callers whose gradients arrive in, and whose parameters leave
+ * through, host memory.  shard->grads[k] and shard->params are HOST pointers
+ * into page-locked memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister);
+ * master, m and v stay DEVICE buffers.  No copy is staged: the fused kernel
+ * reads the contributions and writes the fp16 shard through the host mapping
+ * (on Grace-Blackwell over the coherent NVLink-C2C link), so transfer and
+ * compute overlap in one pass.  The step is then committed on the device as in
+ * zero_shard_step_async, and the call waits for the stream and returns the
+ * step's overflow flag in *overflow_out (HOST).  A host pointer that is not
+ * page-locked and mapped for the current device returns ZS_ERR_ARG before any
+ * launch. */
+ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
+                                    zs_ctrl* ctrl_dev, void* stream, int32_t* overflow_out);
 
 /* params[j] = fp16_rn(master[j]) for j < n (DEVICE buffers): initialises the
  * fp16 parameter slice from fp32 master weights.  Stream-ordered. */

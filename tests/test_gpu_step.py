@@ -31,13 +31,14 @@ class SyncShard:
     """Device buffers of one shard for the synchronous entry point, built from
     host arrays, with the host-side commit bookkeeping."""
 
-    def __init__(self, zs, dev, contribs, master0, n, offset=0, inplace=False):
+    def __init__(self, zs, dev, contribs, master0, n, offset=0, inplace=False, off_h=None, off_f=None):
         self.zs = zs
-        n_alloc = n + offset
-        self.g = [torch.zeros(n_alloc + 8, dtype=torch.float16, device=dev)[offset:offset + n] for _ in contribs]
+        oh = offset if off_h is None else off_h
+        of = offset if off_f is None else off_f
+        self.g = [torch.zeros(n + oh + 16, dtype=torch.float16, device=dev)[oh:oh + n] for _ in contribs]
         for t, c in zip(self.g, contribs):
             t.copy_(c.to(dev))
-        mk = lambda: torch.zeros(n_alloc + 8, dtype=torch.float32, device=dev)[offset:offset + n]
+        mk = lambda: torch.zeros(n + of + 16, dtype=torch.float32, device=dev)[of:of + n]
         self.master = (mk(), None)
         self.master[0].copy_(master0.to(dev))
         self.master = (self.master[0], self.master[0] if inplace else mk())
@@ -45,7 +46,7 @@ class SyncShard:
         self.m = (a, a if inplace else mk())
         b = mk()
         self.v = (b, b if inplace else mk())
-        self.params = torch.zeros(n_alloc + 8, dtype=torch.float16, device=dev)[offset:offset + n]
+        self.params = torch.zeros(n + oh + 16, dtype=torch.float16, device=dev)[oh:oh + n]
         zs.zero_params_from_master(self.master[0], self.params, n)
         self.view = zs.ShardView(self.g, self.master, self.m, self.v, self.params, n)
         self.cur = 0
@@ -153,6 +154,28 @@ def test_empty_shard(zs, cuda_device):
     assert zs.zero_shard_step([empty], 2, zs.adam(1e-3), 1.0, 1, 0, flag) == 0
     for a, b in zip(before, sh.state()):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("n_d", [4, 8, 64])
+@pytest.mark.parametrize("off_h,off_f,width", [(0, 0, "wide"), (8, 4, "narrow"), (0, 4, "narrow"),
+                                               (1, 0, "scalar"), (0, 1, "scalar")])
+def test_alignment_paths(zs, oracle, cuda_device, n_d, off_h, off_f, width):
+    """The three access widths (16 / 8 elements per thread, scalar) give the
+    oracle's results; offsets pick the width through buffer alignment."""
+    n = 2048 * 9 + 13
+    w = _workload(n, n_d)
+    master0 = synth.master_init(w, n)
+    sh = SyncShard(zs, cuda_device, _contribs(w, n, 1), master0, n, off_h=off_h, off_f=off_f)
+    assert (sh.master[0].data_ptr() % 32 == 0) == (off_f == 0)
+    ref = OracleShard(oracle, master0.numpy())
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    for step in (1, 2):
+        contribs = _contribs(w, n, step)
+        sh.set_grads(contribs)
+        assert zs.zero_shard_step([sh.view], n_d, zs.adam(w.lr), w.loss_scale, step, sh.cur, flag) == 0
+        oracle_group_step(oracle, [ref], [_bits(contribs)], w, w.loss_scale, step - 1)
+        sh.cur ^= 1
+        ref.compare(*sh.state(), what=f"{width} n_d={n_d} step={step}")
 
 
 # ----------------------------------------------------- overflow and skip ---
@@ -301,6 +324,46 @@ def test_graph_captured_steps(zs, oracle, cuda_device):
     assert c["step"] == applied == 4
     master, m, v, params = run.current(r)
     ref.compare(to_np(master), to_np(m), to_np(v), f16_bits(params), what="graph")
+
+
+def test_host_memory_path(zs, oracle, cuda_device):
+    """zero_shard_step_host: contributions read from, and the fp16 shard
+    written to, page-locked host memory by the fused kernel."""
+    import ctypes
+    n, n_d = 2048 * 11 + 5, 4
+    w = _workload(n, n_d, numels=(n * n_d,), grads_fresh_per_step=False)
+    run = WorkloadRunner(w, cuda_device)
+    r = run.shard_ids[0]
+    host_grads = [g[:n].cpu().pin_memory() for g in run.grads[r]]
+    host_params = torch.zeros(n, dtype=torch.float16).pin_memory()
+    master, m, v, _ = run.state[r]
+    view = zs.HostShardView(host_grads, master, m, v, host_params, n)
+    ref = OracleShard(oracle, to_np(master[0]))
+    ls, applied = w.loss_scale, 0
+    for step in range(1, 5):
+        if step == 2:
+            saved = host_grads[1][17].clone()
+            host_grads[1][17] = float("inf")
+        host_step = [_bits(host_grads)]
+        ovf = zs.zero_shard_step_host(view, n_d, run.hp, run.ctrl)
+        rovf, ls, applied = oracle_group_step(oracle, [ref], host_step, w, ls, applied)
+        assert ovf == rovf == int(step == 2)
+        if step == 2:
+            host_grads[1][17] = saved
+        c = run.ctrl_host()
+        assert c["step"] == applied and c["loss_scale"] == ls
+        cur = c["cur"]
+        ref.compare(to_np(master[cur]), to_np(m[cur]), to_np(v[cur]), f16_bits(host_params),
+                    what=f"host path step {step}")
+    # pageable host memory is refused before any launch
+    pageable = torch.zeros(n, dtype=torch.float16)
+    bad = zs.Shard.from_buffer_copy(view.struct)
+    bad.params = pageable.data_ptr()
+    out = ctypes.c_int32(-7)
+    launches = zs.zero_kernel_launches()
+    rc = zs.lib().zero_shard_step_host(ctypes.byref(bad), n_d, ctypes.byref(run.hp), run.ctrl.data_ptr(), None,
+                                       ctypes.byref(out))
+    assert rc == zs.ZS_ERR_ARG and zs.zero_kernel_launches() == launches
 
 
 def test_params_from_master_cast(zs, oracle, cuda_device):

@@ -70,6 +70,7 @@ _SIGNATURES = {
     "zero_shard_step": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _P, _P, _P]),
     "zero_ctrl_init": (_I32, [_P, _F64, _P]),
     "zero_shard_step_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
+    "zero_shard_step_host": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "zero_shard_reduce_adam_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
@@ -260,6 +261,39 @@ def zero_shard_step_async(shards: Sequence[ShardView], n_d: int, hp: Adam, ctrl_
     rc = lib().zero_shard_step_async(arr, len(shards), int(n_d), ctypes.byref(hp),
                                      _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
     _check(rc, "zero_shard_step_async")
+
+
+class HostShardView(ShardView):
+    """A shard whose gradient contributions and fp16 slice are page-locked
+    HOST tensors (``tensor.pin_memory()``); master/m/v are CUDA tensors."""
+
+    def __init__(self, grads, master, m, v, params, n):
+        for g in list(grads) + [params]:
+            if g.is_cuda or not g.is_pinned() or g.dtype != torch.float16 or not g.is_contiguous():
+                raise TypeError("host shard: grads and params must be contiguous pinned fp16 host tensors")
+        self.grads = list(grads)
+        self.master, self.m, self.v = tuple(master), tuple(m), tuple(v)
+        self.params = params
+        self.n = int(n)
+        self._table = (_P * max(len(self.grads), 1))(*[g.data_ptr() for g in self.grads])
+        self.struct = Shard()
+        self.struct.grads = ctypes.cast(self._table, ctypes.POINTER(_P))
+        for i in range(2):
+            self.struct.master[i] = _dev_ptr(self.master[i], torch.float32, "master")
+            self.struct.m[i] = _dev_ptr(self.m[i], torch.float32, "m")
+            self.struct.v[i] = _dev_ptr(self.v[i], torch.float32, "v")
+        self.struct.params = params.data_ptr()
+        self.struct.n = self.n
+
+
+def zero_shard_step_host(shard: HostShardView, n_d: int, hp: Adam, ctrl_dev: torch.Tensor, stream=None) -> int:
+    """Step with host-resident contributions and fp16 shard; returns the flag."""
+    ovf = _I32(-1)
+    rc = lib().zero_shard_step_host(ctypes.byref(shard.struct), int(n_d), ctypes.byref(hp),
+                                    _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream),
+                                    ctypes.byref(ovf))
+    _check(rc, "zero_shard_step_host")
+    return int(ovf.value)
 
 
 def zero_shard_reduce_adam_async(shard: ShardView, n_d: int, hp: Adam, ctrl_dev: torch.Tensor, stream=None):

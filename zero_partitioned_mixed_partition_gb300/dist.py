@@ -1,0 +1,42 @@
+"""Host-side multi-rank logic around the shard step.
+
+One process per GPU.  The shards are independent partitions of the parameter
+index set ("DeepSpeed ZeRO Stages", sec. 2.1 Fact 1: the Adam update is
+elementwise), so ranks step their own shards with no exchange on the data
+path.  Two small pieces of host logic cross ranks:
+
+  * the skip decision: an overflow on any rank must skip the step on every
+    rank, so the per-rank flags are ORed (an all-reduce of one int);
+  * timing: the slowest rank's time bounds the job.
+
+Both use ``torch.distributed`` (NCCL on GPUs, gloo on CPU).
+"""
+from __future__ import annotations
+
+import torch
+import torch.distributed as dist
+
+
+def replica_shard(base_rank: int, rank: int, n_d: int) -> int:
+    """Shard stepped by process ``rank`` when every process runs a replica of
+    a workload whose device plays ``base_rank``: consecutive ranks take
+    consecutive shards."""
+    return (int(base_rank) + int(rank)) % int(n_d)
+
+
+def agree_overflow(flag: int, device=None) -> int:
+    """OR of the overflow flags of all ranks (1 if any rank overflowed)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return int(bool(flag))
+    t = torch.tensor([int(bool(flag))], dtype=torch.int32, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return int(t.item())
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the job's time is the slowest rank's)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
