@@ -95,7 +95,7 @@ def test_sync_step_matches_oracle(zs, oracle, cuda_device, n, n_d):
         ref.compare(*sh.state(), what=f"n={n} n_d={n_d} step={step}")
 
 
-@pytest.mark.parametrize("n_d", [2, 5, 16, 17, 64, 65, 100])
+@pytest.mark.parametrize("n_d", [2, 5, 16, 17, 32, 64, 65, 100])
 def test_sync_step_many_contributions(zs, oracle, cuda_device, n_d):
     n = 4099
     w = _workload(n, n_d, loss_scale=float(2 ** 14), grad_mult=float(2 ** 14))
