@@ -92,7 +92,7 @@ def recorded_traffic(kernel_source: str):
                 vals[k.strip()] = v.strip()
         if vals.get("kernel_source_sha256_16") != digest:
             return None
-        return {int(k.split("_")[-1]): float(v) for k, v in vals.items() if k.startswith("bytes_per_param_nd_")}
+        return {int(k.split("_")[-1]): float(v.split()[0]) for k, v in vals.items() if k.startswith("bytes_per_param_nd_")}
     except Exception:
         return None
 
