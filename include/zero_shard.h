@@ -204,6 +204,34 @@ ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t
                                const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
                                int32_t* flag_dev, void* stream, int32_t* overflow_out);
 
+/* Largest n_shards zero_shard_step_noalloc accepts (size of its static scratch). */
+#define ZS_NOALLOC_MAX_SHARDS 64
+
+/* zero_shard_step for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this entry point; it exists for the host program, not
+ * for the method.  Some callers only own the buffers they are handed and may
+ * not call cudaMalloc: a plugin or language binding inside an application whose
+ * allocator has reserved the whole device (a stray allocation would bypass or
+ * fragment that pool, or fail once the pool has claimed the memory), or code
+ * that must not allocate after start-up.  zero_shard_step needs a caller
+ * buffer for its overflow word; this variant keeps one overflow word per shard
+ * in a 256-byte array compiled into the library (each GPU that loads the
+ * library holds it until the process exits) and allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library call.
+ *   - arguments, arithmetic, restore-on-overflow and *overflow_out are those of
+ *     zero_shard_step (without flag_dev);
+ *   - n_shards above ZS_NOALLOC_MAX_SHARDS returns ZS_ERR_ARG (the text is in
+ *     zero_last_error()) and launches nothing;
+ *   - the first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture;
+ *   - every call shares the array, and it keeps the last call's contents; each
+ *     call clears the words it uses before its kernels run.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on it, so
+ *     order them. */
+ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                       const zs_adam* hp, double loss_scale, int64_t step,
+                                       int32_t cur, void* stream, int32_t* overflow_out);
+
 /* Set up a device control block: loss scale L, t = 0, cur = 0, counters 0.
  * Stream-ordered (one tiny kernel). */
 ZS_API int32_t zero_ctrl_init(zs_ctrl* ctrl_dev, double loss_scale, void* stream);

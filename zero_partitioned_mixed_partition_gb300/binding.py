@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libzeroshard.so")
 ZS_OK, ZS_ERR_ARG, ZS_ERR_ALIGN, ZS_ERR_CUDA, ZS_ERR_TIMEOUT = 0, -1, -2, -3, -4
 ZS_MAX_ND = 1024
 ZS_MAX_SHARDS = 256
+ZS_NOALLOC_MAX_SHARDS = 64
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -68,6 +69,7 @@ _SIGNATURES = {
     "zero_partition_layout_device": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P]),
     "zero_state_bytes": (_F64, [_F64, _I32, _I32, _F64]),
     "zero_shard_step": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _P, _P, _P]),
+    "zero_shard_step_noalloc": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _P, _P]),
     "zero_ctrl_init": (_I32, [_P, _F64, _P]),
     "zero_shard_step_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "zero_shard_step_host": (_I32, [_P, _I32, _P, _P, _P, _P]),
@@ -243,6 +245,20 @@ def zero_shard_step(shards: Sequence[ShardView], n_d: int, hp: Adam, loss_scale:
                                int(cur), _dev_ptr(flag_dev, torch.int32, "flag_dev"), _stream(stream),
                                ctypes.byref(ovf))
     _check(rc, "zero_shard_step")
+    return int(ovf.value)
+
+
+def zero_shard_step_noalloc(shards: Sequence[ShardView], n_d: int, hp: Adam, loss_scale: float, step: int,
+                            cur: int, stream=None) -> int:
+    """zero_shard_step without the caller's flag buffer: for callers that may
+    not allocate device memory, the overflow words live in a small array
+    compiled into the library.  Returns the overflow flag (0/1)."""
+    arr = _shard_array(shards)
+    ovf = _I32(-1)
+    rc = lib().zero_shard_step_noalloc(arr, len(shards), int(n_d), ctypes.byref(hp), float(loss_scale),
+                                       int(step), int(cur), _stream(stream), ctypes.byref(ovf))
+    if rc != ZS_OK:
+        raise ZeroShardError(rc, "zero_shard_step_noalloc", zero_last_error())
     return int(ovf.value)
 
 

@@ -21,6 +21,11 @@ int32_t cuda_fail(cudaError_t err, const char* where) {
     return ZS_ERR_CUDA;
 }
 
+int32_t fail_with(int32_t status, const char* message) {
+    g_last_error = message;
+    return status;
+}
+
 void count_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int device_sm_count() {

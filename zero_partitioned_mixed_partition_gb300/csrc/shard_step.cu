@@ -621,6 +621,87 @@ ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t
     return ZS_OK;
 }
 
+// ------------------------------------------------ no-allocation entry point ---
+
+// Overflow words of zero_shard_step_noalloc, one per shard of a call.  Lives in
+// the library image: every device that loads the library has its own copy for
+// the life of the process.  Host code must not use the symbol as an address;
+// noalloc_scratch() looks up the device address.
+static __device__ __align__(256) int32_t g_noalloc_scratch[ZS_NOALLOC_MAX_SHARDS];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+static int32_t* noalloc_scratch(int32_t* status) {
+    static std::mutex mu;
+    static std::unordered_map<int, int32_t*> by_device;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) {
+        *status = zs::cuda_fail(err, "zero_shard_step_noalloc: cudaGetDevice");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = by_device.find(dev);
+    if (it != by_device.end()) return it->second;
+    void* addr = nullptr;
+    err = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (err != cudaSuccess || addr == nullptr) {
+        *status = zs::cuda_fail(err != cudaSuccess ? err : cudaErrorInvalidSymbol,
+                                "zero_shard_step_noalloc: cudaGetSymbolAddress");
+        return nullptr;
+    }
+    by_device[dev] = static_cast<int32_t*>(addr);
+    return by_device[dev];
+}
+
+ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                       const zs_adam* hp, double loss_scale, int64_t step,
+                                       int32_t cur, void* stream, int32_t* overflow_out) {
+    if (n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || !(loss_scale > 0.0) || loss_scale > 1e300 ||
+        step < 1 || (cur != 0 && cur != 1) || overflow_out == nullptr)
+        return ZS_ERR_ARG;
+    if (n_shards > ZS_NOALLOC_MAX_SHARDS)
+        return zs::fail_with(ZS_ERR_ARG, "zero_shard_step_noalloc: n_shards exceeds ZS_NOALLOC_MAX_SHARDS "
+                                         "(the size of its static scratch)");
+    int width[ZS_NOALLOC_MAX_SHARDS];
+    int32_t rc = check_shard_list(shards, n_shards, n_d, width);
+    if (rc != ZS_OK) return rc;
+    int32_t* scratch = noalloc_scratch(&rc);
+    if (scratch == nullptr) return rc;
+
+    double p1 = 1.0, p2 = 1.0;
+    for (int64_t i = 0; i < step; ++i) {
+        p1 *= hp->beta1;
+        p2 *= hp->beta2;
+    }
+    const Coef coef = coef_host(*hp, p1, p2, n_d, loss_scale);
+    cudaStream_t st = (cudaStream_t)stream;
+    // the array keeps the previous call's words: clear the ones this call uses
+    cudaError_t err = cudaMemsetAsync(scratch, 0, sizeof(int32_t) * n_shards, st);
+    if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_noalloc: clear scratch");
+    for (int32_t i = 0; i < n_shards; ++i) {
+        if (shards[i].n == 0) continue;
+        rc = launch_step(shards[i], n_d, width[i], &coef, cur, *hp, nullptr, scratch + i, st);
+        if (rc != ZS_OK) return rc;
+    }
+    int32_t words[ZS_NOALLOC_MAX_SHARDS];
+    err = cudaMemcpyAsync(words, scratch, sizeof(int32_t) * n_shards, cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_noalloc: read scratch");
+    int32_t flag = 0;
+    for (int32_t i = 0; i < n_shards; ++i) flag |= words[i];
+    if (flag) {
+        for (int32_t i = 0; i < n_shards; ++i) {
+            rc = launch_cast(shards[i].master[cur], shards[i].params, shards[i].n, st);
+            if (rc != ZS_OK) return rc;
+        }
+        err = cudaStreamSynchronize(st);
+        if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_noalloc: restore");
+    }
+    *overflow_out = flag ? 1 : 0;
+    return ZS_OK;
+}
+
 ZS_API int32_t zero_ctrl_init(zs_ctrl* ctrl_dev, double loss_scale, void* stream) {
     if (ctrl_dev == nullptr || !(loss_scale > 0.0) || loss_scale > 1e300) return ZS_ERR_ARG;
     if (!zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;

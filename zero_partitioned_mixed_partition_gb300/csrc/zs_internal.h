@@ -11,6 +11,8 @@ namespace zs {
 
 // Records a CUDA failure for zero_last_error() and returns ZS_ERR_CUDA.
 int32_t cuda_fail(cudaError_t err, const char* where);
+// Records a message for zero_last_error() and returns status.
+int32_t fail_with(int32_t status, const char* message);
 // Adds n to the count reported by zero_kernel_launches().
 void count_launches(int64_t n);
 
