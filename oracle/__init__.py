@@ -78,6 +78,12 @@ def _load():
             lib.oracle_shard_step.restype = _I32
             lib.oracle_commit.argtypes = [_I32, _P, _P]
             lib.oracle_commit.restype = None
+            lib.oracle_grad_sqnorm.argtypes = [_P, _I64, _P]
+            lib.oracle_grad_sqnorm.restype = None
+            lib.oracle_clip_factor.argtypes = [_F64, _F64]
+            lib.oracle_clip_factor.restype = ctypes.c_float
+            lib.oracle_scale.argtypes = [_P, _I64, ctypes.c_float]
+            lib.oracle_scale.restype = None
             _lib = lib
     return _lib
 
@@ -205,3 +211,25 @@ def commit(overflow: int, loss_scale: float, applied_steps: int):
     ls, st = _F64(loss_scale), _I64(applied_steps)
     _load().oracle_commit(int(overflow), ctypes.byref(ls), ctypes.byref(st))
     return ls.value, st.value
+
+
+# ------------------------------------------------------------ clipping ---
+
+def grad_sqnorm(g, start: float = 0.0) -> float:
+    """start + sum of g_j^2 (float64, index order) over float32 gradients."""
+    g = _contig(g, np.float32)
+    acc = _F64(start)
+    _load().oracle_grad_sqnorm(_ptr(g), g.size, ctypes.byref(acc))
+    return acc.value
+
+
+def clip_factor(sqnorm: float, max_norm: float) -> float:
+    """min(1, max_norm / (sqrt(sqnorm) + 1e-6)) rounded to float32."""
+    return float(_load().oracle_clip_factor(float(sqnorm), float(max_norm)))
+
+
+def scale(g, c: float):
+    """g *= c in float32, in place."""
+    if g.dtype != np.float32 or not g.flags.c_contiguous:
+        raise TypeError("g must be contiguous float32")
+    _load().oracle_scale(_ptr(g), g.size, ctypes.c_float(c))

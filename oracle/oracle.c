@@ -27,6 +27,10 @@
  *                         and "The per-step mechanics", beat 3)
  *   oracle_shard_step    the two above for one shard with the skip rule
  *   oracle_commit        skip / commit bookkeeping after an overflow test
+ *   oracle_grad_sqnorm,  global gradient-norm clipping: the squared norm of
+ *   oracle_clip_factor,  the reduced gradient, the clip factor and the
+ *   oracle_scale         scaled gradient ("DeepSpeed ZeRO Stages" sec. 2.1,
+ *                        Fact 1: clipping needs ||g||_2 over all of P)
  *
  * Precision.  The pages fix the precisions: fp16 gradients and parameters,
  * fp32 master weights, m and v ("ZeRO Stage 1 Math", "The 16-bytes-per-
@@ -45,7 +49,11 @@
  *     multiply by (float)(1 / (N_d * L)) for loss scale L;
  *   - overflow: any non-finite reduced gradient in the valid range skips the
  *     whole step; the loss scale halves, never below 1; no growth;
- *   - fp32 -> fp16 rounding is IEEE round-to-nearest-even.
+ *   - fp32 -> fp16 rounding is IEEE round-to-nearest-even;
+ *   - clipping (the pages name it, give no formula): ||g||_2 over every
+ *     shard of the reduced, unscaled gradient, summed in double;
+ *     c = min(1, max_norm / (||g||_2 + 1e-6)) in double, rounded once to
+ *     float, and g' = g * c in fp32 before the Adam update.
  *
  * Parity pins for every function live in the tests (closed forms and worked
  * values printed on the pages, exhaustive fp16 checks against numpy, the
@@ -319,4 +327,36 @@ void oracle_commit(int32_t overflow, double* loss_scale, int64_t* applied_steps)
     } else {
         *applied_steps += 1;
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Global gradient-norm clipping.                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Adds sum_j g_j^2 over n reduced gradients to *sqnorm, in double, in index
+ * order.  (A float squared is exact in double.)  Clipping couples every
+ * coordinate through ||g||_2 over all of P ("DeepSpeed ZeRO Stages",
+ * sec. 2.1, Fact 1), so each rank adds its shard and the ranks sum. */
+void oracle_grad_sqnorm(const float* g, int64_t n, double* sqnorm)
+{
+    double acc = *sqnorm;
+    for (int64_t j = 0; j < n; ++j) acc = acc + (double)g[j] * (double)g[j];
+    *sqnorm = acc;
+}
+
+/* Clip factor for a global squared norm: min(1, max_norm / (||g|| + 1e-6)),
+ * formed in double and rounded once to float.  max_norm <= 0 disables
+ * clipping (factor 1). */
+float oracle_clip_factor(double sqnorm, double max_norm)
+{
+    if (!(max_norm > 0.0)) return 1.0f;
+    double c = max_norm / (sqrt(sqnorm) + 1e-6);
+    if (!(c < 1.0)) c = 1.0;
+    return (float)c;
+}
+
+/* g_j <- g_j * c in fp32. */
+void oracle_scale(float* g, int64_t n, float c)
+{
+    for (int64_t j = 0; j < n; ++j) g[j] = g[j] * c;
 }
