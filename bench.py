@@ -46,6 +46,10 @@ def parse_args():
                     help="shrink the workload to this many params per shard (profiling runs)")
     ap.add_argument("--prewarm-s", type=float, default=3.0,
                     help="seconds of untimed steps before the warm-up steps (HBM power ramp)")
+    ap.add_argument("--clip", type=float, default=0.0,
+                    help="global gradient-norm clipping at this max norm (two-pass step); 0 = off")
+    ap.add_argument("--clip-keep-g", action="store_true",
+                    help="with --clip: pass 1 keeps the fp32 reduced gradient for pass 2")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-mode", default="mapped", choices=["mapped", "staged"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -264,15 +268,35 @@ def main():
         lay_frags = torch.zeros(cap * 4, dtype=torch.int64, device=dev)
     torch.cuda.synchronize()
 
-    def one_step(ev_pair=None):
+    clip = args.clip > 0
+    if clip:
+        run.enable_clipping(args.clip_keep_g)
+
+    def one_step(ev=None):
         binding.zero_partition_layout_device(numels_dev, w.n_d, w.align, lay_scalars, lay_toff, lay_soff,
                                              lay_frags, cap, stream=stream)
-        if ev_pair is not None:
-            ev_pair[0].record(stream)
-        for i in range(len(run.views)):
-            run.reduce_adam(i)
-        if ev_pair is not None:
-            ev_pair[1].record(stream)
+        if not clip:
+            if ev is not None:
+                ev[0].record(stream)
+            for i in range(len(run.views)):
+                run.reduce_adam(i)
+            if ev is not None:
+                ev[1].record(stream)
+        else:
+            with torch.cuda.stream(stream):
+                run.sqnorm.zero_()
+            if ev is not None:
+                ev[0].record(stream)
+            for i, view in enumerate(run.views):
+                binding.zero_shard_grad_sqnorm_async(view, w.n_d, run.sqnorm, run.ctrl,
+                                                     g_dev=run.gbuf[i] if run.gbuf else None, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+            for i, view in enumerate(run.views):
+                binding.zero_shard_clipped_adam_async(view, w.n_d, run.hp, args.clip, run.sqnorm, run.ctrl,
+                                                      g_dev=run.gbuf[i] if run.gbuf else None, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
         run.commit()
 
     # untimed pre-warm: the first seconds of sustained HBM traffic after idle
@@ -290,8 +314,7 @@ def main():
     lay = lay_scalars.cpu().tolist()
     assert lay[4] == 0 and lay[2] == run.S, lay
 
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(args.steps)]
+    pairs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -309,7 +332,10 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     ms_total = t_start.elapsed_time(t_end)
-    kern_ms = [a.elapsed_time(b) for a, b in pairs]
+    kern_ms = [ev[0].elapsed_time(ev[1]) for ev in pairs]
+    if clip:
+        norm_ms = [ev[0].elapsed_time(ev[2]) for ev in pairs]
+        upd_ms = [ev[2].elapsed_time(ev[1]) for ev in pairs]
     ctrl = run.ctrl_host()
     assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + args.warmup + args.steps, ctrl
 
@@ -317,7 +343,7 @@ def main():
     elems = run.elements_per_step()
     total_elems = elems * world
     value = total_elems * args.steps / (ms_max / 1e3) / 1e9
-    bytes_step = run.bytes_per_step()
+    bytes_step = run.clipped_bytes_per_step() if clip else run.bytes_per_step()
     hbm_gbs = bytes_step * world * args.steps / (ms_max / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
 
@@ -327,8 +353,21 @@ def main():
     traffic_per_param = recorded_traffic(os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc",
                                                       "shard_step.cu"))
     traffic = None
-    if traffic_per_param and w.n_d in traffic_per_param:
+    if traffic_per_param and w.n_d in traffic_per_param and not clip:
         traffic = round(traffic_per_param[w.n_d] * elems)
+    clip_info = None
+    if clip:
+        # per pass: algorithmic bytes / mean launch time (pass 1 reads the
+        # contributions, writes g if kept; pass 2 reads g or re-reduces)
+        b1 = (2 * w.n_d + (4 if run.gbuf else 0)) * elems
+        b2 = ((4 if run.gbuf else 2 * w.n_d) + 26) * elems
+        clip_info = {"max_norm": args.clip, "keep_g": bool(run.gbuf),
+                     "bytes_per_param": (2 * w.n_d + 34) if run.gbuf else (4 * w.n_d + 26),
+                     "norm_pass": {"ms_mean": round(statistics.mean(norm_ms), 5),
+                                   "gbs": round(b1 / (statistics.mean(norm_ms) / 1e3) / 1e9, 1)},
+                     "update_pass": {"ms_mean": round(statistics.mean(upd_ms), 5),
+                                     "gbs": round(b2 / (statistics.mean(upd_ms) / 1e3) / 1e9, 1)},
+                     "sqnorm_last": float(run.sqnorm.item())}
 
     # end to end through the C ABI with host buffers: pinned H2D of the step's
     # gradient contributions, the step, D2H of the fp16 shard and the control block
@@ -359,6 +398,9 @@ def main():
         "gpu_launches": int(launches),
         "e2e": e2e,
     }
+    if clip_info is not None:
+        line["clip"] = clip_info
+        line["roofline"]["kernel"] = "grad_norm_kernel + clipped_step_kernel"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         g, steps, el, th = oracle_throughput(w, min(4_000_000, elems), args.cpu_seconds, os.cpu_count() or 1)
         line["cpu_baseline"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th, "kind": "oracle",

@@ -275,6 +275,43 @@ ZS_API int32_t zero_step_commit_async(const zs_shard* shards, int32_t n_shards, 
 ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
                                     zs_ctrl* ctrl_dev, void* stream, int32_t* overflow_out);
 
+/* ------------------------------------------------------------------------ */
+/* Global gradient-norm clipping ("DeepSpeed ZeRO Stages", sec. 2.1, Fact 1:   */
+/* the one operation of the step that couples coordinates, through ||g||_2   */
+/* over all of P, at the price of one scalar all-reduce).                    */
+/* ------------------------------------------------------------------------ */
+/* With clipping the step takes two passes around one scalar S = sum_j g_j^2
+ * over every shard of every rank (g the reduced, unscaled gradient of
+ * zero_shard_step):
+ *   1. zero_shard_grad_sqnorm_async on each local shard: reduce, ORs the
+ *      non-finite test into ctrl->overflow and ADDS the shard's sum of
+ *      squares (double) to *sqnorm_dev (DEVICE, 8-byte aligned; the caller
+ *      clears it before the step).  g_dev (DEVICE fp32, >= n values, or NULL)
+ *      keeps g for pass 2.
+ *   2. the ranks sum *sqnorm_dev (one-double all-reduce); shards stepped on
+ *      one device are already summed.
+ *   3. zero_shard_clipped_adam_async on each shard: c = min(1, max_norm /
+ *      (sqrt(S) + 1e-6)) in double, rounded once to float (max_norm <= 0: no
+ *      clipping), g' = g * c in fp32, then the update and fp16 cast of
+ *      zero_shard_step with g'.  g is read from g_dev, or re-reduced from the
+ *      contributions when g_dev is NULL (same bits).
+ *   4. zero_step_commit_async for all the shards.
+ * Per element: 4 n_d + 26 bytes without g_dev, 2 n_d + 34 with it; keep g
+ * once n_d > 4.  Loss scale, t and the ping-pong set come from *ctrl_dev as in
+ * zero_shard_step_async. */
+ZS_API int32_t zero_shard_grad_sqnorm_async(const zs_shard* shard, int32_t n_d, float* g_dev,
+                                            double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
+ZS_API int32_t zero_shard_clipped_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
+                                             double max_norm, const float* g_dev,
+                                             const double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
+/* Steps 1-4 for shards that all live on this device (the norm is then exact
+ * over them): clears *sqnorm_dev, runs pass 1 over every shard, pass 2 over
+ * every shard, and the commit.  g_dev: HOST array of n_shards DEVICE
+ * pointers (each may be NULL), or NULL to re-reduce everywhere. */
+ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                             const zs_adam* hp, double max_norm, float* const* g_dev,
+                                             double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
+
 /* params[j] = fp16_rn(master[j]) for j < n (DEVICE buffers): initialises the
  * fp16 parameter slice from fp32 master weights.  Stream-ordered. */
 ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params_dev, int64_t n,

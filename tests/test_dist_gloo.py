@@ -58,6 +58,20 @@ def _worker(rank, world, port, q):
         out["flags"] = flags
         out["master"] = (lo, master)
         out["ls"], out["applied"] = ls, applied
+
+        # global gradient clipping: each rank adds its shard's sum of squares,
+        # the ranks sum them, and every rank clips with the same factor
+        cm, cmm, cv = theta[lo:hi].copy(), np.zeros(hi - lo, np.float32), np.zeros(hi - lo, np.float32)
+        for step in range(2):
+            parts = [c[lo:hi].view(np.uint16) for c in contrib[2 * step]]
+            g, bad = oracle.grad_reduce(parts, 256.0)
+            sq = torch.tensor([oracle.grad_sqnorm(g)], dtype=torch.float64)
+            zdist.allreduce_sqnorm(sq)
+            c = oracle.clip_factor(float(sq.item()), 5.0)
+            oracle.scale(g, c)
+            oracle.adam_apply(g, cm, cmm, cv, None, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                              weight_decay=0.0, step=step + 1)
+        out["clip_sq"], out["clip_c"], out["clip_master"] = float(sq.item()), c, (lo, cm)
         q.put((rank, out))
     finally:
         dist.destroy_process_group()
@@ -100,3 +114,20 @@ def test_two_ranks_agree_on_skip_and_time():
         lo, part = res[r]["master"]
         joined[lo:lo + part.size] = part
     assert np.array_equal(joined, master)
+
+    # clipped steps: the summed norm and the joined shards match one unsharded run
+    cm, cmm, cv = theta.copy(), np.zeros(psi, np.float32), np.zeros(psi, np.float32)
+    for step in range(2):
+        g, _ = oracle.grad_reduce([c.view(np.uint16) for c in contrib[2 * step]], 256.0)
+        sq = oracle.grad_sqnorm(g)
+        c = oracle.clip_factor(sq, 5.0)
+        oracle.scale(g, c)
+        oracle.adam_apply(g, cm, cmm, cv, None, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+                          step=step + 1)
+    assert res[0]["clip_sq"] == res[1]["clip_sq"] and abs(res[0]["clip_sq"] - sq) <= 1e-12 * sq
+    assert res[0]["clip_c"] == res[1]["clip_c"] == c and c < 1.0
+    joined = np.zeros(psi, np.float32)
+    for r in range(world):
+        lo, part = res[r]["clip_master"]
+        joined[lo:lo + part.size] = part
+    np.testing.assert_allclose(joined, cm, rtol=2e-6, atol=1e-9)

@@ -18,6 +18,13 @@ from parity_util import (OracleShard, assert_f16_close, assert_f32_close, f16_bi
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _fresh_ulp_record():
+    """test_report_max_ulp summarises this module's comparisons only."""
+    MAX_ULP["f32"] = MAX_ULP["f16"] = 0
+    yield
+
+
 def _workload(n, n_d, **kw):
     base = dict(name="case", numels=(n,), n_d=n_d, rank=0, align=1, steps=3, lr=1e-3, beta1=0.9,
                 beta2=0.999, eps=1e-8, weight_decay=0.0, loss_scale=1024.0, grad_dist="normal",

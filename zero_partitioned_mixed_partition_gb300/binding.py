@@ -74,6 +74,9 @@ _SIGNATURES = {
     "zero_shard_step_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "zero_shard_step_host": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "zero_shard_reduce_adam_async": (_I32, [_P, _I32, _P, _P, _P]),
+    "zero_shard_grad_sqnorm_async": (_I32, [_P, _I32, _P, _P, _P, _P]),
+    "zero_shard_clipped_adam_async": (_I32, [_P, _I32, _P, _F64, _P, _P, _P, _P]),
+    "zero_shard_step_clipped_async": (_I32, [_P, _I32, _I32, _P, _F64, _P, _P, _P, _P]),
     "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
     "zero_status_string": (ctypes.c_char_p, [_I32]),
@@ -323,6 +326,45 @@ def zero_step_commit_async(shards: Sequence[ShardView], hp: Adam, ctrl_dev: torc
     rc = lib().zero_step_commit_async(arr, len(shards), ctypes.byref(hp),
                                       _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
     _check(rc, "zero_step_commit_async")
+
+
+def new_sqnorm(device="cuda") -> torch.Tensor:
+    """Device accumulator for the squared gradient norm (one float64)."""
+    return torch.zeros(1, dtype=torch.float64, device=device)
+
+
+def zero_shard_grad_sqnorm_async(shard: ShardView, n_d: int, sqnorm_dev: torch.Tensor, ctrl_dev: torch.Tensor,
+                                 g_dev: Optional[torch.Tensor] = None, stream=None):
+    """Clipping pass 1 for one shard: adds its sum of squares to sqnorm_dev."""
+    rc = lib().zero_shard_grad_sqnorm_async(ctypes.byref(shard.struct), int(n_d),
+                                            _dev_ptr(g_dev, torch.float32, "g_dev"),
+                                            _dev_ptr(sqnorm_dev, torch.float64, "sqnorm_dev"),
+                                            _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_grad_sqnorm_async")
+
+
+def zero_shard_clipped_adam_async(shard: ShardView, n_d: int, hp: Adam, max_norm: float, sqnorm_dev: torch.Tensor,
+                                  ctrl_dev: torch.Tensor, g_dev: Optional[torch.Tensor] = None, stream=None):
+    """Clipping pass 2 for one shard: clipped update and fp16 cast."""
+    rc = lib().zero_shard_clipped_adam_async(ctypes.byref(shard.struct), int(n_d), ctypes.byref(hp),
+                                             float(max_norm), _dev_ptr(g_dev, torch.float32, "g_dev"),
+                                             _dev_ptr(sqnorm_dev, torch.float64, "sqnorm_dev"),
+                                             _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_clipped_adam_async")
+
+
+def zero_shard_step_clipped_async(shards: Sequence[ShardView], n_d: int, hp: Adam, max_norm: float,
+                                  sqnorm_dev: torch.Tensor, ctrl_dev: torch.Tensor,
+                                  g_dev: Optional[Sequence[Optional[torch.Tensor]]] = None, stream=None):
+    """Whole clipped step over shards that all live on this device."""
+    arr = _shard_array(shards)
+    table = None
+    if g_dev is not None:
+        table = (_P * len(shards))(*[_dev_ptr(g, torch.float32, "g_dev") for g in g_dev])
+    rc = lib().zero_shard_step_clipped_async(arr, len(shards), int(n_d), ctypes.byref(hp), float(max_norm), table,
+                                             _dev_ptr(sqnorm_dev, torch.float64, "sqnorm_dev"),
+                                             _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_step_clipped_async")
 
 
 def zero_params_from_master(master: torch.Tensor, params: torch.Tensor, n: int, stream=None):

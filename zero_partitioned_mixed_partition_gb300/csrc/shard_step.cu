@@ -37,168 +37,7 @@ constexpr int kThreads = 256;          // threads per block of the fused kernel
 constexpr int kCommitThreads = 512;    // threads per block of the commit kernel
 constexpr int kCastThreads = 256;
 
-// ------------------------------------------------------------ coefficients ---
-
-// Scalar coefficients of one step, each formed in double and rounded once to
-// float, so host and device agree bit for bit.
-struct Coef {
-    float b1, c1, b2, c2;  // beta1, 1 - beta1, beta2, 1 - beta2
-    float bc1, bc2;        // 1 - beta1^t, 1 - beta2^t
-    float lr, eps, wd;
-    float inv;             // 1 / (N_d L)
-};
-
-Coef coef_host(const zs_adam& hp, double p1, double p2, int n_d, double loss_scale) {
-    Coef c;
-    c.b1 = (float)hp.beta1;
-    c.c1 = (float)(1.0 - hp.beta1);
-    c.b2 = (float)hp.beta2;
-    c.c2 = (float)(1.0 - hp.beta2);
-    c.bc1 = (float)(1.0 - p1);
-    c.bc2 = (float)(1.0 - p2);
-    c.lr = (float)hp.lr;
-    c.eps = (float)hp.eps;
-    c.wd = (float)hp.weight_decay;
-    c.inv = (float)(1.0 / ((double)n_d * loss_scale));
-    return c;
-}
-
-__device__ Coef coef_device(const zs_adam& hp, double p1, double p2, int n_d, double loss_scale) {
-    Coef c;
-    c.b1 = __double2float_rn(hp.beta1);
-    c.c1 = __double2float_rn(__dsub_rn(1.0, hp.beta1));
-    c.b2 = __double2float_rn(hp.beta2);
-    c.c2 = __double2float_rn(__dsub_rn(1.0, hp.beta2));
-    c.bc1 = __double2float_rn(__dsub_rn(1.0, p1));
-    c.bc2 = __double2float_rn(__dsub_rn(1.0, p2));
-    c.lr = __double2float_rn(hp.lr);
-    c.eps = __double2float_rn(hp.eps);
-    c.wd = __double2float_rn(hp.weight_decay);
-    c.inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)n_d, loss_scale)));
-    return c;
-}
-
-// ------------------------------------------------------------ element math ---
-
-__device__ __forceinline__ bool nonfinite(float x) {
-    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
-}
-
-// One Adam / AdamW update of one coordinate from its summed gradient gs.
-__device__ __forceinline__ void adam_update(const Coef& c, float gs, float& th, float& m, float& v) {
-    const float g = __fmul_rn(gs, c.inv);
-    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.c1, g));
-    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.c2, __fmul_rn(g, g)));
-    const float mh = __fdiv_rn(m, c.bc1);
-    const float vh = __fdiv_rn(v, c.bc2);
-    const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), c.eps));
-    th = __fsub_rn(th, __fmul_rn(c.lr, __fadd_rn(u, __fmul_rn(c.wd, th))));
-}
-
-// --------------------------------------------------------- vector memory ---
-
-// How a thread moves its VEC consecutive elements per loop iteration.
-//   Mem<8>   "narrow": one 16-byte fp16 access per contribution, two 16-byte
-//            fp32 accesses per state array, all with evict-first (.cs) hints.
-//            Needs 16-byte aligned buffers.  Best measured layout for small
-//            N_d (N_d <= 4: 6.65 TB/s on a 375M-param shard).
-//   Mem<16>  "wide": two 16-byte fp16 accesses per contribution and one
-//            256-bit (v8) fp32 access per 8 state values, default caching.
-//            Twice the contribution bytes in flight per thread, which large
-//            N_d needs (N_d = 64: 7.06 TB/s vs 4.98 TB/s narrow).  Needs
-//            32-byte aligned fp32 buffers and 16-byte aligned fp16 buffers.
-//   Mem<1>   scalar, any naturally aligned buffer.
-template <int VEC> struct Mem;
-
-template <> struct Mem<8> {
-    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
-        const uint4 r = __ldcs(reinterpret_cast<const uint4*>(p));
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            out[2 * i] = f.x;
-            out[2 * i + 1] = f.y;
-        }
-    }
-    static __device__ __forceinline__ void load_f(const float* p, float* out) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-        const float4 b = __ldcs(reinterpret_cast<const float4*>(p + 4));
-        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
-    }
-    static __device__ __forceinline__ void store_f(float* p, const float* in) {
-        __stcs(reinterpret_cast<float4*>(p), make_float4(in[0], in[1], in[2], in[3]));
-        __stcs(reinterpret_cast<float4*>(p + 4), make_float4(in[4], in[5], in[6], in[7]));
-    }
-    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2 h = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
-            w[i] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        __stcs(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
-    }
-};
-
-template <> struct Mem<16> {
-    static __device__ __forceinline__ void load_h8(const uint16_t* p, float* out) {
-        const uint4 r = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            out[2 * i] = f.x;
-            out[2 * i + 1] = f.y;
-        }
-    }
-    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
-        load_h8(p, out);
-        load_h8(p + 8, out + 8);
-    }
-    static __device__ __forceinline__ void load_f8(const float* p, float* o) {
-        asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]), "=f"(o[4]), "=f"(o[5]), "=f"(o[6]),
-                       "=f"(o[7])
-                     : "l"(p));
-    }
-    static __device__ __forceinline__ void load_f(const float* p, float* out) {
-        load_f8(p, out);
-        load_f8(p + 8, out + 8);
-    }
-    static __device__ __forceinline__ void store_f8(float* p, const float* v) {
-        asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                     :: "l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
-                        "f"(v[7])
-                     : "memory");
-    }
-    static __device__ __forceinline__ void store_f(float* p, const float* in) {
-        store_f8(p, in);
-        store_f8(p + 8, in + 8);
-    }
-    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const __half2 h = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
-            w[i] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(p + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-};
-
-template <> struct Mem<1> {
-    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
-        out[0] = __half2float(__ushort_as_half(__ldcs(reinterpret_cast<const unsigned short*>(p))));
-    }
-    static __device__ __forceinline__ void load_f(const float* p, float* out) { out[0] = __ldcs(p); }
-    static __device__ __forceinline__ void store_f(float* p, const float* in) { __stcs(p, in[0]); }
-    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
-        __stcs(reinterpret_cast<unsigned short*>(p), __half_as_ushort(__float2half_rn(in[0])));
-    }
-};
+#include "step_common.cuh"
 
 // ------------------------------------------------------------ fused kernel ---
 
@@ -220,33 +59,6 @@ struct StepArgs {
     int32_t* flag;        // overflow accumulator (ORed)
 };
 
-// Unroll of the contribution loop when N_d is a compile-time constant above 16.
-constexpr int kUnrollLargeNd = 8;
-
-// Sum of the N_d contributions of VEC consecutive elements, in rank order.
-// ND > 0: exactly ND contributions, known at compile time (fully unrolled for
-// ND <= 16, unrolled by kUnrollLargeNd above); ND == 0: p.n_d of them (<= CAP),
-// unrolled by 4.
-template <int CAP, int VEC, int ND>
-__device__ __forceinline__ void sum_contributions(const StepArgs<CAP>& p, int64_t e, float* acc) {
-    auto add = [&](int k) {
-        float h[VEC];
-        Mem<VEC>::load_h(p.grads[k] + e, h);
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[j] = __fadd_rn(acc[j], h[j]);
-    };
-    if constexpr (ND > 0 && ND <= 16) {
-#pragma unroll
-        for (int k = 0; k < ND; ++k) add(k);
-    } else if constexpr (ND > 16) {
-#pragma unroll kUnrollLargeNd
-        for (int k = 0; k < ND; ++k) add(k);
-    } else {
-#pragma unroll 4
-        for (int k = 0; k < p.n_d; ++k) add(k);
-    }
-}
-
 // VEC elements of the shard starting at element e: reduce, test, update, cast.
 template <int CAP, int VEC, int ND>
 __device__ __forceinline__ uint32_t step_elements(const StepArgs<CAP>& p, const Coef& c, int64_t e,
@@ -259,7 +71,7 @@ __device__ __forceinline__ uint32_t step_elements(const StepArgs<CAP>& p, const 
     Mem<VEC>::load_f(v_in + e, v);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
-    sum_contributions<CAP, VEC, ND>(p, e, acc);
+    sum_contributions<CAP, VEC, ND>(p.grads, p.n_d, e, acc);
     uint32_t bad = 0;
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
@@ -412,6 +224,11 @@ __global__ void ctrl_init_kernel(zs_ctrl* ctrl, double loss_scale) {
     *ctrl = c;
 }
 
+
+}  // namespace
+
+namespace zs {
+
 // ------------------------------------------------------------ host helpers ---
 
 // Persistent grid: enough blocks to fill every SM at the kernel's occupancy,
@@ -473,6 +290,57 @@ int32_t check_shard(const zs_shard& s, int32_t n_d, int* width) {
     return ZS_OK;
 }
 
+template <int MAXS>
+int32_t launch_commit_cap(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
+                          cudaStream_t stream) {
+    CommitArgs<MAXS> a;
+    for (int i = 0; i < MAXS; ++i) {
+        if (i < n_shards) {
+            a.shards[i].params = shards[i].params;
+            a.shards[i].master[0] = shards[i].master[0];
+            a.shards[i].master[1] = shards[i].master[1];
+            a.shards[i].n = shards[i].n;
+        } else {
+            a.shards[i] = CommitShard{nullptr, {nullptr, nullptr}, 0};
+        }
+    }
+    a.n_shards = n_shards;
+    a.beta1 = hp.beta1;
+    a.beta2 = hp.beta2;
+    a.ctrl = ctrl;
+    // one block per SM: enough to restore the slices at full bandwidth on an
+    // overflow step, few enough that a normal step costs only the arrivals
+    const int blocks = zs::device_sm_count();
+    commit_kernel<MAXS><<<blocks, kCommitThreads, 0, stream>>>(a);
+    return zs::check_launch("commit_kernel");
+}
+
+int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
+                      cudaStream_t stream) {
+    if (n_shards <= 1) return launch_commit_cap<1>(shards, n_shards, hp, ctrl, stream);
+    if (n_shards <= 16) return launch_commit_cap<16>(shards, n_shards, hp, ctrl, stream);
+    return launch_commit_cap<ZS_MAX_SHARDS>(shards, n_shards, hp, ctrl, stream);
+}
+
+int32_t check_shard_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, int* width) {
+    if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS) return ZS_ERR_ARG;
+    for (int32_t i = 0; i < n_shards; ++i) {
+        int32_t rc = check_shard(shards[i], n_d, &width[i]);
+        if (rc != ZS_OK) return rc;
+    }
+    return ZS_OK;
+}
+
+}  // namespace zs
+
+using zs::check_shard;
+using zs::check_shard_list;
+using zs::launch_commit;
+using zs::persistent_blocks;
+using zs::valid_hp;
+
+namespace {
+
 template <int CAP, int VEC, int ND>
 int32_t launch_step_vec(const StepArgs<CAP>& a, cudaStream_t stream) {
     const void* k = (const void*)shard_step_kernel<CAP, VEC, ND>;
@@ -532,47 +400,6 @@ int32_t launch_cast(const float* master, uint16_t* params, int64_t n, cudaStream
     const int blocks = persistent_blocks((const void*)cast_kernel, kCastThreads, (n + 7) / 8);
     cast_kernel<<<blocks, kCastThreads, 0, stream>>>(master, params, n);
     return zs::check_launch("cast_kernel");
-}
-
-template <int MAXS>
-int32_t launch_commit_cap(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
-                          cudaStream_t stream) {
-    CommitArgs<MAXS> a;
-    for (int i = 0; i < MAXS; ++i) {
-        if (i < n_shards) {
-            a.shards[i].params = shards[i].params;
-            a.shards[i].master[0] = shards[i].master[0];
-            a.shards[i].master[1] = shards[i].master[1];
-            a.shards[i].n = shards[i].n;
-        } else {
-            a.shards[i] = CommitShard{nullptr, {nullptr, nullptr}, 0};
-        }
-    }
-    a.n_shards = n_shards;
-    a.beta1 = hp.beta1;
-    a.beta2 = hp.beta2;
-    a.ctrl = ctrl;
-    // one block per SM: enough to restore the slices at full bandwidth on an
-    // overflow step, few enough that a normal step costs only the arrivals
-    const int blocks = zs::device_sm_count();
-    commit_kernel<MAXS><<<blocks, kCommitThreads, 0, stream>>>(a);
-    return zs::check_launch("commit_kernel");
-}
-
-int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
-                      cudaStream_t stream) {
-    if (n_shards <= 1) return launch_commit_cap<1>(shards, n_shards, hp, ctrl, stream);
-    if (n_shards <= 16) return launch_commit_cap<16>(shards, n_shards, hp, ctrl, stream);
-    return launch_commit_cap<ZS_MAX_SHARDS>(shards, n_shards, hp, ctrl, stream);
-}
-
-int32_t check_shard_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, int* width) {
-    if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS) return ZS_ERR_ARG;
-    for (int32_t i = 0; i < n_shards; ++i) {
-        int32_t rc = check_shard(shards[i], n_d, &width[i]);
-        if (rc != ZS_OK) return rc;
-    }
-    return ZS_OK;
 }
 
 }  // namespace

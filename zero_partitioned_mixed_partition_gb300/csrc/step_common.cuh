@@ -1,0 +1,201 @@
+// step_common.cuh -- device code shared by the kernels of libzeroshard.so:
+// the step coefficients, the element update and the vector memory accesses.
+// Each CUDA translation unit includes it inside its anonymous namespace, after
+// <cuda_fp16.h>, <stdint.h> and zero_shard.h.
+#pragma once
+
+// ------------------------------------------------------------ coefficients ---
+
+// Scalar coefficients of one step, each formed in double and rounded once to
+// float, so host and device agree bit for bit.
+struct Coef {
+    float b1, c1, b2, c2;  // beta1, 1 - beta1, beta2, 1 - beta2
+    float bc1, bc2;        // 1 - beta1^t, 1 - beta2^t
+    float lr, eps, wd;
+    float inv;             // 1 / (N_d L)
+};
+
+Coef coef_host(const zs_adam& hp, double p1, double p2, int n_d, double loss_scale) {
+    Coef c;
+    c.b1 = (float)hp.beta1;
+    c.c1 = (float)(1.0 - hp.beta1);
+    c.b2 = (float)hp.beta2;
+    c.c2 = (float)(1.0 - hp.beta2);
+    c.bc1 = (float)(1.0 - p1);
+    c.bc2 = (float)(1.0 - p2);
+    c.lr = (float)hp.lr;
+    c.eps = (float)hp.eps;
+    c.wd = (float)hp.weight_decay;
+    c.inv = (float)(1.0 / ((double)n_d * loss_scale));
+    return c;
+}
+
+__device__ Coef coef_device(const zs_adam& hp, double p1, double p2, int n_d, double loss_scale) {
+    Coef c;
+    c.b1 = __double2float_rn(hp.beta1);
+    c.c1 = __double2float_rn(__dsub_rn(1.0, hp.beta1));
+    c.b2 = __double2float_rn(hp.beta2);
+    c.c2 = __double2float_rn(__dsub_rn(1.0, hp.beta2));
+    c.bc1 = __double2float_rn(__dsub_rn(1.0, p1));
+    c.bc2 = __double2float_rn(__dsub_rn(1.0, p2));
+    c.lr = __double2float_rn(hp.lr);
+    c.eps = __double2float_rn(hp.eps);
+    c.wd = __double2float_rn(hp.weight_decay);
+    c.inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)n_d, loss_scale)));
+    return c;
+}
+
+// ------------------------------------------------------------ element math ---
+
+__device__ __forceinline__ bool nonfinite(float x) {
+    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
+}
+
+// One Adam / AdamW update of one coordinate from its reduced gradient g.
+__device__ __forceinline__ void adam_apply(const Coef& c, float g, float& th, float& m, float& v) {
+    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.c1, g));
+    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.c2, __fmul_rn(g, g)));
+    const float mh = __fdiv_rn(m, c.bc1);
+    const float vh = __fdiv_rn(v, c.bc2);
+    const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), c.eps));
+    th = __fsub_rn(th, __fmul_rn(c.lr, __fadd_rn(u, __fmul_rn(c.wd, th))));
+}
+
+// The same from the summed contributions gs: g = gs * (float)(1 / (N_d L)).
+__device__ __forceinline__ void adam_update(const Coef& c, float gs, float& th, float& m, float& v) {
+    adam_apply(c, __fmul_rn(gs, c.inv), th, m, v);
+}
+
+// --------------------------------------------------------- vector memory ---
+
+// How a thread moves its VEC consecutive elements per loop iteration.
+//   Mem<8>   "narrow": one 16-byte fp16 access per contribution, two 16-byte
+//            fp32 accesses per state array, all with evict-first (.cs) hints.
+//            Needs 16-byte aligned buffers.  Best measured layout for small
+//            N_d (N_d <= 4: 6.65 TB/s on a 375M-param shard).
+//   Mem<16>  "wide": two 16-byte fp16 accesses per contribution and one
+//            256-bit (v8) fp32 access per 8 state values, default caching.
+//            Twice the contribution bytes in flight per thread, which large
+//            N_d needs (N_d = 64: 7.06 TB/s vs 4.98 TB/s narrow).  Needs
+//            32-byte aligned fp32 buffers and 16-byte aligned fp16 buffers.
+//   Mem<1>   scalar, any naturally aligned buffer.
+template <int VEC> struct Mem;
+
+template <> struct Mem<8> {
+    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
+        const uint4 r = __ldcs(reinterpret_cast<const uint4*>(p));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void load_f(const float* p, float* out) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(p + 4));
+        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    }
+    static __device__ __forceinline__ void store_f(float* p, const float* in) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(in[0], in[1], in[2], in[3]));
+        __stcs(reinterpret_cast<float4*>(p + 4), make_float4(in[4], in[5], in[6], in[7]));
+    }
+    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        __stcs(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
+    }
+};
+
+template <> struct Mem<16> {
+    static __device__ __forceinline__ void load_h8(const uint16_t* p, float* out) {
+        const uint4 r = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
+        load_h8(p, out);
+        load_h8(p + 8, out + 8);
+    }
+    static __device__ __forceinline__ void load_f8(const float* p, float* o) {
+        asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]), "=f"(o[4]), "=f"(o[5]), "=f"(o[6]),
+                       "=f"(o[7])
+                     : "l"(p));
+    }
+    static __device__ __forceinline__ void load_f(const float* p, float* out) {
+        load_f8(p, out);
+        load_f8(p + 8, out + 8);
+    }
+    static __device__ __forceinline__ void store_f8(float* p, const float* v) {
+        asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                     :: "l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+                        "f"(v[7])
+                     : "memory");
+    }
+    static __device__ __forceinline__ void store_f(float* p, const float* in) {
+        store_f8(p, in);
+        store_f8(p + 8, in + 8);
+    }
+    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const __half2 h = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(p + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+};
+
+template <> struct Mem<1> {
+    static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
+        out[0] = __half2float(__ushort_as_half(__ldcs(reinterpret_cast<const unsigned short*>(p))));
+    }
+    static __device__ __forceinline__ void load_f(const float* p, float* out) { out[0] = __ldcs(p); }
+    static __device__ __forceinline__ void store_f(float* p, const float* in) { __stcs(p, in[0]); }
+    static __device__ __forceinline__ void store_h(uint16_t* p, const float* in) {
+        __stcs(reinterpret_cast<unsigned short*>(p), __half_as_ushort(__float2half_rn(in[0])));
+    }
+};
+
+// Unroll of the contribution loop when N_d is a compile-time constant above 16.
+constexpr int kUnrollLargeNd = 8;
+
+// Sum of the N_d contributions of VEC consecutive elements, in rank order.
+// ND > 0: exactly ND contributions, known at compile time (fully unrolled for
+// ND <= 16, unrolled by kUnrollLargeNd above); ND == 0: p.n_d of them (<= CAP),
+// unrolled by 4.
+template <int CAP, int VEC, int ND>
+__device__ __forceinline__ void sum_contributions(const uint16_t* const (&grads)[CAP], int n_d, int64_t e,
+                                                  float* acc) {
+    auto add = [&](int k) {
+        float h[VEC];
+        Mem<VEC>::load_h(grads[k] + e, h);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[j] = __fadd_rn(acc[j], h[j]);
+    };
+    if constexpr (ND > 0 && ND <= 16) {
+#pragma unroll
+        for (int k = 0; k < ND; ++k) add(k);
+    } else if constexpr (ND > 16) {
+#pragma unroll kUnrollLargeNd
+        for (int k = 0; k < ND; ++k) add(k);
+    } else {
+#pragma unroll 4
+        for (int k = 0; k < n_d; ++k) add(k);
+    }
+}
+

@@ -29,4 +29,17 @@ inline int32_t check_launch(const char* where, int64_t n = 1) {
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Persistent grid for `kernel`: every SM filled at the kernel's occupancy, no
+// more blocks than work_items / threads.
+int persistent_blocks(const void* kernel, int threads, int64_t work_items);
+// Hyper-parameters finite, betas in [0, 1), eps >= 0.
+bool valid_hp(const zs_adam* hp);
+// Checks one shard's pointers; *width gets the access width they allow
+// (2 = 16 elements per thread, 1 = 8, 0 = scalar).
+int32_t check_shard(const zs_shard& s, int32_t n_d, int* width);
+int32_t check_shard_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, int* width);
+// Enqueues the device-side commit / skip of a step over `shards`.
+int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
+                      cudaStream_t stream);
+
 }  // namespace zs

@@ -3,13 +3,15 @@
 One process per GPU.  The shards are independent partitions of the parameter
 index set ("DeepSpeed ZeRO Stages", sec. 2.1 Fact 1: the Adam update is
 elementwise), so ranks step their own shards with no exchange on the data
-path.  Two small pieces of host logic cross ranks:
+path.  Small pieces of host logic cross ranks:
 
   * the skip decision: an overflow on any rank must skip the step on every
     rank, so the per-rank flags are ORed (an all-reduce of one int);
+  * with global gradient clipping, the squared gradient norm: each rank adds
+    its shard's sum of squares and the ranks sum them (one double);
   * timing: the slowest rank's time bounds the job.
 
-Both use ``torch.distributed`` (NCCL on GPUs, gloo on CPU).
+All use ``torch.distributed`` (NCCL on GPUs, gloo on CPU).
 """
 from __future__ import annotations
 
@@ -31,6 +33,14 @@ def agree_overflow(flag: int, device=None) -> int:
     t = torch.tensor([int(bool(flag))], dtype=torch.int32, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return int(t.item())
+
+
+def allreduce_sqnorm(sqnorm: torch.Tensor) -> torch.Tensor:
+    """Sum the ranks' squared-gradient-norm accumulators in place (the one
+    scalar exchange global gradient clipping adds to the step)."""
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(sqnorm, op=dist.ReduceOp.SUM)
+    return sqnorm
 
 
 def max_over_ranks(value: float, device=None) -> float:

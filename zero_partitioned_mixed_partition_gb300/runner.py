@@ -73,6 +73,25 @@ class WorkloadRunner:
     def commit(self):
         binding.zero_step_commit_async(self.views, self.hp, self.ctrl, stream=self.stream)
 
+    def enable_clipping(self, keep_g: bool):
+        """Allocate the squared-norm accumulator (and, with keep_g, one fp32
+        buffer per shard for the reduced gradient kept between the passes)."""
+        self.sqnorm = binding.new_sqnorm(self.device)
+        self.gbuf = None
+        if keep_g:
+            self.gbuf = [torch.zeros(self.S, dtype=torch.float32, device=self.device) for _ in self.shard_ids]
+
+    def step_clipped(self, max_norm: float):
+        """One clipped step over every stepped shard, stream-ordered."""
+        binding.zero_shard_step_clipped_async(self.views, self.w.n_d, self.hp, max_norm, self.sqnorm, self.ctrl,
+                                              g_dev=self.gbuf, stream=self.stream)
+
+    def clipped_bytes_per_step(self) -> int:
+        """Algorithmic HBM bytes of one clipped step: 4 N_d + 26 per element
+        when pass 2 re-reduces, 2 N_d + 34 when it reads the kept g."""
+        per = (2 * self.w.n_d + 34) if self.gbuf is not None else (4 * self.w.n_d + 26)
+        return sum(per * self.n_valid[r] for r in self.shard_ids)
+
     def refresh_grads(self, step: int):
         """Draw the contributions of ``step`` (workloads with fresh gradients)."""
         for r in self.shard_ids:
