@@ -84,6 +84,10 @@ def _load():
             lib.oracle_clip_factor.restype = ctypes.c_float
             lib.oracle_scale.argtypes = [_P, _I64, ctypes.c_float]
             lib.oracle_scale.restype = None
+            lib.oracle_qwz_quantize.argtypes = [_P, _I64, _P, _P]
+            lib.oracle_qwz_quantize.restype = None
+            lib.oracle_qwz_dequantize.argtypes = [_P, _P, _I64, _P]
+            lib.oracle_qwz_dequantize.restype = None
             _lib = lib
     return _lib
 
@@ -233,3 +237,26 @@ def scale(g, c: float):
     if g.dtype != np.float32 or not g.flags.c_contiguous:
         raise TypeError("g must be contiguous float32")
     _load().oracle_scale(_ptr(g), g.size, ctypes.c_float(c))
+
+
+# -------------------------------------------------- quantized weights ---
+
+QWZ_BLOCK = 256
+
+
+def qwz_quantize(params_bits):
+    """int8 codes and float32 per-block scales of uint16 fp16 parameters."""
+    p = _contig(params_bits, np.uint16)
+    codes = np.empty(p.size, np.int8)
+    scales = np.empty((p.size + QWZ_BLOCK - 1) // QWZ_BLOCK, np.float32)
+    _load().oracle_qwz_quantize(_ptr(p), p.size, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def qwz_dequantize(codes, scales):
+    """uint16 fp16 parameters rebuilt from codes and scales."""
+    c = _contig(codes, np.int8)
+    s = _contig(scales, np.float32)
+    out = np.empty(c.size, np.uint16)
+    _load().oracle_qwz_dequantize(_ptr(c), _ptr(s), c.size, _ptr(out))
+    return out

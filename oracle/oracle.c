@@ -31,6 +31,11 @@
  *   oracle_clip_factor,  the reduced gradient, the clip factor and the
  *   oracle_scale         scaled gradient ("DeepSpeed ZeRO Stages" sec. 2.1,
  *                        Fact 1: clipping needs ||g||_2 over all of P)
+ *   oracle_qwz_quantize, block-wise int8 quantization of the fp16 shard for
+ *   oracle_qwz_dequantize the parameter all-gather and its inverse
+ *                        ("ZeRO Optimization: Stages 1, 2, and 3 Explained",
+ *                         ZeRO++ quantized weights; "DeepSpeed ZeRO Stages"
+ *                         sec. 5.3, qwZ)
  *
  * Precision.  The pages fix the precisions: fp16 gradients and parameters,
  * fp32 master weights, m and v ("ZeRO Stage 1 Math", "The 16-bytes-per-
@@ -53,7 +58,12 @@
  *   - clipping (the pages name it, give no formula): ||g||_2 over every
  *     shard of the reduced, unscaled gradient, summed in double;
  *     c = min(1, max_norm / (||g||_2 + 1e-6)) in double, rounded once to
- *     float, and g' = g * c in fp32 before the Adam update.
+ *     float, and g' = g * c in fp32 before the Adam update;
+ *   - quantized weights (the pages give blocks with their own scale, 16 -> 8
+ *     bit, nothing more): blocks of 256 consecutive parameters of the shard,
+ *     the last one possibly shorter; scale = max|x| / 127 in fp32;
+ *     q = rint(x / scale) (ties to even) in fp32, 0 when the scale is 0;
+ *     the receiver rebuilds fp16(q * scale).
  *
  * Parity pins for every function live in the tests (closed forms and worked
  * values printed on the pages, exhaustive fp16 checks against numpy, the
@@ -359,4 +369,44 @@ float oracle_clip_factor(double sqnorm, double max_norm)
 void oracle_scale(float* g, int64_t n, float c)
 {
     for (int64_t j = 0; j < n; ++j) g[j] = g[j] * c;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantized parameter all-gather (ZeRO++ qwZ).                              */
+/* ------------------------------------------------------------------------ */
+
+#define ORACLE_QWZ_BLOCK 256
+
+/* Block-wise symmetric int8 quantization of n fp16 parameters: for each block
+ * of 256 consecutive values (the last one may be shorter) scale = max|x| / 127
+ * and q = rint(x / scale), both in fp32 ("ZeRO Optimization: Stages 1, 2, and
+ * 3 Explained", ZeRO++: 16-bit parameters sent as 8-bit with a scale per
+ * small block).  codes[n], scales[ceil(n / 256)]. */
+void oracle_qwz_quantize(const uint16_t* params, int64_t n, int8_t* codes, float* scales)
+{
+    for (int64_t b = 0; b * ORACLE_QWZ_BLOCK < n; ++b) {
+        int64_t lo = b * ORACLE_QWZ_BLOCK;
+        int64_t hi = lo + ORACLE_QWZ_BLOCK < n ? lo + ORACLE_QWZ_BLOCK : n;
+        float amax = 0.0f;
+        for (int64_t j = lo; j < hi; ++j) {
+            float a = fabsf(oracle_f16_to_f32(params[j]));
+            if (a > amax) amax = a;
+        }
+        float scale = amax / 127.0f;
+        scales[b] = scale;
+        for (int64_t j = lo; j < hi; ++j) {
+            float q = 0.0f;
+            if (scale > 0.0f) q = rintf(oracle_f16_to_f32(params[j]) / scale);
+            if (q > 127.0f) q = 127.0f;
+            if (q < -127.0f) q = -127.0f;
+            codes[j] = (int8_t)q;
+        }
+    }
+}
+
+/* The receiver's side: params[j] = fp16(q_j * scale_of_its_block). */
+void oracle_qwz_dequantize(const int8_t* codes, const float* scales, int64_t n, uint16_t* params)
+{
+    for (int64_t j = 0; j < n; ++j)
+        params[j] = oracle_f32_to_f16((float)codes[j] * scales[j / ORACLE_QWZ_BLOCK]);
 }
