@@ -50,6 +50,8 @@ def parse_args():
                     help="global gradient-norm clipping at this max norm (two-pass step); 0 = off")
     ap.add_argument("--clip-keep-g", action="store_true",
                     help="with --clip: pass 1 keeps the fp32 reduced gradient for pass 2")
+    ap.add_argument("--qwz", action="store_true",
+                    help="keep the int8 qwZ copy of the fp16 shard in each step (1 + 4/256 bytes per element)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-mode", default="mapped", choices=["mapped", "staged"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -271,6 +273,8 @@ def main():
     clip = args.clip > 0
     if clip:
         run.enable_clipping(args.clip_keep_g)
+    if args.qwz:
+        run.enable_qwz()
 
     def one_step(ev=None):
         binding.zero_partition_layout_device(numels_dev, w.n_d, w.align, lay_scalars, lay_toff, lay_soff,
@@ -344,6 +348,8 @@ def main():
     total_elems = elems * world
     value = total_elems * args.steps / (ms_max / 1e3) / 1e9
     bytes_step = run.clipped_bytes_per_step() if clip else run.bytes_per_step()
+    if args.qwz:  # int8 codes + one fp32 scale per 256 elements, written by the step
+        bytes_step += sum(run.n_valid[r] + 4 * ((run.n_valid[r] + 255) // 256) for r in run.shard_ids)
     hbm_gbs = bytes_step * world * args.steps / (ms_max / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
 
@@ -353,7 +359,7 @@ def main():
     traffic_per_param = recorded_traffic(os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc",
                                                       "shard_step.cu"))
     traffic = None
-    if traffic_per_param and w.n_d in traffic_per_param and not clip:
+    if traffic_per_param and w.n_d in traffic_per_param and not clip and not args.qwz:
         traffic = round(traffic_per_param[w.n_d] * elems)
     clip_info = None
     if clip:
@@ -382,7 +388,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
-                   "bytes_per_param": 26 + 2 * w.n_d, "bytes_per_step": bytes_step,
+                   "bytes_per_param": round(bytes_step / max(elems, 1), 4), "bytes_per_step": bytes_step,
                    "storage": "fp16 grads and params, fp32 master/m/v (ping-pong)",
                    "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
                    if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number",
@@ -398,6 +404,8 @@ def main():
         "gpu_launches": int(launches),
         "e2e": e2e,
     }
+    if args.qwz:
+        line["qwz"] = {"block": 256, "extra_bytes_per_param": round(1 + 4 / 256, 4)}
     if clip_info is not None:
         line["clip"] = clip_info
         line["roofline"]["kernel"] = "grad_norm_kernel + clipped_step_kernel"

@@ -59,6 +59,8 @@ extern "C" {
 #define ZS_MAX_ND 1024
 /* Largest number of shards one step may update together. */
 #define ZS_MAX_SHARDS 256
+/* Parameters per block of the int8 (qwZ) copy of the fp16 shard. */
+#define ZS_QWZ_BLOCK 256
 
 /* One piece of the partition: the overlap of one tensor with one shard. */
 typedef struct zs_fragment {
@@ -97,7 +99,20 @@ typedef struct zs_adam {
  * every fp16 buffer 16-byte aligned the kernel moves 16 elements per thread
  * and iteration (used when n_d > 4); with 16-byte alignment, 8; any other
  * 4-byte (fp32) / 2-byte (fp16) aligned layout takes a scalar kernel.  All
- * three do the same arithmetic in the same order. */
+ * three do the same arithmetic in the same order.
+ *   qcodes, qscales
+ *             optional (both NULL, or both set): the int8 copy of the fp16
+ *             shard that the parameter all-gather sends instead of fp16
+ *             (ZeRO++ quantized weights, "ZeRO Optimization: Stages 1, 2, and
+ *             3 Explained"; "DeepSpeed ZeRO Stages" sec. 5.3 qwZ).  DEVICE
+ *             int8 codes[n] and fp32 scales[ceil(n / ZS_QWZ_BLOCK)]: block b
+ *             holds params [256 b, 256 b + 256) as q = rint(x / s), ties to
+ *             even, s = max|x| / 127, x the fp16 values.  When set, every
+ *             step (and every restore after an overflow) leaves them matching
+ *             the fp16 slice; the fused kernel writes full blocks in its own
+ *             pass (1 + 4/256 extra bytes per element) and the commit writes
+ *             the trailing partial block.  codes 16-byte aligned for the
+ *             16-element path, 8-byte for the 8-element one. */
 typedef struct zs_shard {
     const uint16_t* const* grads;
     float* master[2];
@@ -105,6 +120,8 @@ typedef struct zs_shard {
     float* v[2];
     uint16_t* params;
     int64_t n;
+    int8_t* qcodes;
+    float* qscales;
 } zs_shard;
 
 /* Device-resident step state for the stream-ordered (no host sync) path.
@@ -316,6 +333,19 @@ ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_s
  * fp16 parameter slice from fp32 master weights.  Stream-ordered. */
 ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params_dev, int64_t n,
                                        void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Quantized weights (qwZ) on their own.                                     */
+/* ------------------------------------------------------------------------ */
+
+/* codes / scales (DEVICE) of n fp16 params (DEVICE), by the rule of
+ * zs_shard.qcodes.  Stream-ordered. */
+ZS_API int32_t zero_qwz_quantize(const uint16_t* params_dev, int64_t n, int8_t* codes_dev,
+                                 float* scales_dev, void* stream);
+/* The all-gather receiver's side: params[j] = fp16_rn(codes[j] * scales[j / 256])
+ * (DEVICE buffers).  Stream-ordered. */
+ZS_API int32_t zero_qwz_dequantize(const int8_t* codes_dev, const float* scales_dev, int64_t n,
+                                   uint16_t* params_dev, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Diagnostics.                                                              */

@@ -23,6 +23,7 @@ ZS_OK, ZS_ERR_ARG, ZS_ERR_ALIGN, ZS_ERR_CUDA, ZS_ERR_TIMEOUT = 0, -1, -2, -3, -4
 ZS_MAX_ND = 1024
 ZS_MAX_SHARDS = 256
 ZS_NOALLOC_MAX_SHARDS = 64
+ZS_QWZ_BLOCK = 256
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -47,7 +48,7 @@ class Adam(ctypes.Structure):
 
 class Shard(ctypes.Structure):
     _fields_ = [("grads", ctypes.POINTER(_P)), ("master", _P * 2), ("m", _P * 2), ("v", _P * 2),
-                ("params", _P), ("n", _I64)]
+                ("params", _P), ("n", _I64), ("qcodes", _P), ("qscales", _P)]
 
 
 class Ctrl(ctypes.Structure):
@@ -79,6 +80,8 @@ _SIGNATURES = {
     "zero_shard_step_clipped_async": (_I32, [_P, _I32, _I32, _P, _F64, _P, _P, _P, _P]),
     "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
+    "zero_qwz_quantize": (_I32, [_P, _I64, _P, _P, _P]),
+    "zero_qwz_dequantize": (_I32, [_P, _P, _I64, _P, _P]),
     "zero_status_string": (ctypes.c_char_p, [_I32]),
     "zero_last_error": (ctypes.c_char_p, []),
     "zero_kernel_launches": (_I64, []),
@@ -204,9 +207,11 @@ class ShardView:
     grads: list of n_d fp16 CUDA tensors (each >= n elements);
     master, m, v: pairs (set 0, set 1) of fp32 CUDA tensors (the same tensor
     twice means in-place); params: fp16 CUDA tensor (the shard's slice of the
-    full parameter buffer); n: elements stepped."""
+    full parameter buffer); n: elements stepped; qcodes / qscales: optional
+    int8 / fp32 CUDA tensors for the qwZ copy of the fp16 slice."""
 
-    def __init__(self, grads: Sequence[torch.Tensor], master, m, v, params: torch.Tensor, n: int):
+    def __init__(self, grads: Sequence[torch.Tensor], master, m, v, params: torch.Tensor, n: int,
+                 qcodes: Optional[torch.Tensor] = None, qscales: Optional[torch.Tensor] = None):
         self.grads = list(grads)
         self.master, self.m, self.v = tuple(master), tuple(m), tuple(v)
         self.params = params
@@ -221,6 +226,14 @@ class ShardView:
             self.struct.v[i] = _dev_ptr(self.v[i], torch.float32, "v")
         self.struct.params = _dev_ptr(params, torch.float16, "params")
         self.struct.n = self.n
+        self.qcodes, self.qscales = qcodes, qscales
+        if (qcodes is None) != (qscales is None):
+            raise ValueError("qcodes and qscales go together")
+        if qcodes is not None:
+            if qcodes.numel() < self.n or qscales.numel() < (self.n + ZS_QWZ_BLOCK - 1) // ZS_QWZ_BLOCK:
+                raise ValueError("qwZ buffers too small")
+            self.struct.qcodes = _dev_ptr(qcodes, torch.int8, "qcodes")
+            self.struct.qscales = _dev_ptr(qscales, torch.float32, "qscales")
 
     @property
     def n_d(self) -> int:
@@ -283,10 +296,11 @@ def zero_shard_step_async(shards: Sequence[ShardView], n_d: int, hp: Adam, ctrl_
 
 
 class HostShardView(ShardView):
-    """A shard whose gradient contributions and fp16 slice are page-locked
-    HOST tensors (``tensor.pin_memory()``); master/m/v are CUDA tensors."""
+    """A shard whose gradient contributions and fp16 slice (and optional qwZ
+    copy) are page-locked HOST tensors (``tensor.pin_memory()``); master/m/v
+    are CUDA tensors."""
 
-    def __init__(self, grads, master, m, v, params, n):
+    def __init__(self, grads, master, m, v, params, n, qcodes=None, qscales=None):
         for g in list(grads) + [params]:
             if g.is_cuda or not g.is_pinned() or g.dtype != torch.float16 or not g.is_contiguous():
                 raise TypeError("host shard: grads and params must be contiguous pinned fp16 host tensors")
@@ -303,6 +317,13 @@ class HostShardView(ShardView):
             self.struct.v[i] = _dev_ptr(self.v[i], torch.float32, "v")
         self.struct.params = params.data_ptr()
         self.struct.n = self.n
+        self.qcodes, self.qscales = qcodes, qscales
+        if qcodes is not None:
+            for t in (qcodes, qscales):
+                if t.is_cuda or not t.is_pinned():
+                    raise TypeError("host shard: qwZ buffers must be pinned host tensors")
+            self.struct.qcodes = qcodes.data_ptr()
+            self.struct.qscales = qscales.data_ptr()
 
 
 def zero_shard_step_host(shard: HostShardView, n_d: int, hp: Adam, ctrl_dev: torch.Tensor, stream=None) -> int:
@@ -371,6 +392,21 @@ def zero_params_from_master(master: torch.Tensor, params: torch.Tensor, n: int, 
     rc = lib().zero_params_from_master(_dev_ptr(master, torch.float32, "master"),
                                        _dev_ptr(params, torch.float16, "params"), int(n), _stream(stream))
     _check(rc, "zero_params_from_master")
+
+
+def zero_qwz_quantize(params: torch.Tensor, n: int, codes: torch.Tensor, scales: torch.Tensor, stream=None):
+    """int8 codes and per-256 fp32 scales of an fp16 slice (stream-ordered)."""
+    rc = lib().zero_qwz_quantize(_dev_ptr(params, torch.float16, "params"), int(n),
+                                 _dev_ptr(codes, torch.int8, "codes"), _dev_ptr(scales, torch.float32, "scales"),
+                                 _stream(stream))
+    _check(rc, "zero_qwz_quantize")
+
+
+def zero_qwz_dequantize(codes: torch.Tensor, scales: torch.Tensor, n: int, params: torch.Tensor, stream=None):
+    """fp16 slice rebuilt from int8 codes and scales (the all-gather receiver)."""
+    rc = lib().zero_qwz_dequantize(_dev_ptr(codes, torch.int8, "codes"), _dev_ptr(scales, torch.float32, "scales"),
+                                   int(n), _dev_ptr(params, torch.float16, "params"), _stream(stream))
+    _check(rc, "zero_qwz_dequantize")
 
 
 def read_ctrl(ctrl_dev: torch.Tensor) -> dict:

@@ -229,8 +229,8 @@ int32_t launch_cap(Pass pass, const zs_shard& s, int32_t n_d, int width, float* 
     return launch_pass<CAP, 1, ND>(pass, a, stream);
 }
 
-int32_t launch(Pass pass, const zs_shard& s, int32_t n_d, int width, float* g, double* sqnorm, double max_norm,
-               const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+int32_t launch_by_nd(Pass pass, const zs_shard& s, int32_t n_d, int width, float* g, double* sqnorm,
+                     double max_norm, const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
     switch (n_d) {
     case 16: return launch_cap<16, 16>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
     case 32: return launch_cap<32, 32>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
@@ -241,6 +241,17 @@ int32_t launch(Pass pass, const zs_shard& s, int32_t n_d, int width, float* g, d
     if (n_d <= 16) return launch_cap<16, 0>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
     if (n_d <= 64) return launch_cap<64, 0>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
     return launch_cap<ZS_MAX_ND, 0>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+}
+
+// Pass 1 or 2 for one shard; after pass 2 the shard's qwZ copy (if any) is
+// rebuilt from the new fp16 slice in its own pass (3 + 4/256 bytes per element).
+int32_t launch(Pass pass, const zs_shard& s, int32_t n_d, int width, float* g, double* sqnorm, double max_norm,
+               const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+    int32_t rc = launch_by_nd(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    if (rc == ZS_OK && pass == Pass::Update && s.qcodes != nullptr)
+        rc = zs::launch_qwz(nullptr, s.params, s.n, s.qcodes, s.qscales, 0, (s.n + kQwzBlock - 1) / kQwzBlock,
+                            stream);
+    return rc;
 }
 
 // Width allowed by the shard together with its kept-g buffer (fp32 like the state).

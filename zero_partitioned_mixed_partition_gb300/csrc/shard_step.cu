@@ -57,15 +57,18 @@ struct StepArgs {
     zs_adam hp;           // hyper-parameters for device-resolved coefficients
     const zs_ctrl* ctrl;  // non-null: loss scale, t and cur come from here
     int32_t* flag;        // overflow accumulator (ORed)
+    int8_t* qcodes;       // qwZ copy (QZ kernels only)
+    float* qscales;
 };
 
 // VEC elements of the shard starting at element e: reduce, test, update, cast.
+// The updated master values are left in th.
 template <int CAP, int VEC, int ND>
 __device__ __forceinline__ uint32_t step_elements(const StepArgs<CAP>& p, const Coef& c, int64_t e,
                                                   const float* th_in, const float* m_in,
                                                   const float* v_in, float* th_out, float* m_out,
-                                                  float* v_out) {
-    float th[VEC], m[VEC], v[VEC], acc[VEC];
+                                                  float* v_out, float* th) {
+    float m[VEC], v[VEC], acc[VEC];
     Mem<VEC>::load_f(th_in + e, th);
     Mem<VEC>::load_f(m_in + e, m);
     Mem<VEC>::load_f(v_in + e, v);
@@ -85,7 +88,7 @@ __device__ __forceinline__ uint32_t step_elements(const StepArgs<CAP>& p, const 
     return bad;
 }
 
-template <int CAP, int VEC, int ND>
+template <int CAP, int VEC, int ND, bool QZ>
 __global__ void __launch_bounds__(kThreads) shard_step_kernel(const __grid_constant__ StepArgs<CAP> p) {
     __shared__ Coef s_coef;
     __shared__ int s_cur;
@@ -114,12 +117,40 @@ __global__ void __launch_bounds__(kThreads) shard_step_kernel(const __grid_const
     uint32_t bad = 0;
     const int64_t nvec = p.n / VEC;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
-        bad |= step_elements<CAP, VEC, ND>(p, c, i * VEC, th_in, m_in, v_in, th_out, m_out, v_out);
+    if constexpr (!QZ) {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+            float th[VEC];
+            bad |= step_elements<CAP, VEC, ND>(p, c, i * VEC, th_in, m_in, v_in, th_out, m_out, v_out, th);
+        }
+    } else {
+        // qwZ: whole warps iterate together so that the G lanes holding one
+        // 256-parameter block can reduce its max by shuffles; every full block
+        // gets its codes and scale here, the trailing partial one in the commit
+        static_assert(VEC == 8 || VEC == 16, "qwZ needs the vector layouts");
+        constexpr int G = kQwzBlock / VEC;
+        const int lane = threadIdx.x & 31;
+        for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < nvec; i0 += stride) {
+            const int64_t i = i0 + lane;
+            const bool active = i < nvec;
+            float th[VEC], x[VEC];
+            if (active) bad |= step_elements<CAP, VEC, ND>(p, c, i * VEC, th_in, m_in, v_in, th_out, m_out, v_out, th);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) x[j] = active ? as_fp16_value(th[j]) : 0.0f;
+            int8_t q[VEC];
+            const float scale = qwz_group_codes<VEC, G>(x, active ? VEC : 0, q);
+            const int64_t block = (i0 + (lane & ~(G - 1))) * VEC / kQwzBlock;
+            if ((block + 1) * kQwzBlock <= p.n) {  // full block: every lane of the group is active
+                store_codes<VEC>(p.qcodes + i * VEC, q);
+                if ((lane & (G - 1)) == 0) p.qscales[block] = scale;
+            }
+        }
+    }
     if (VEC > 1) {  // ragged tail: fewer than VEC elements, one per thread of block 0
         const int64_t e = nvec * VEC + threadIdx.x;
-        if (blockIdx.x == 0 && e < p.n)
-            bad |= step_elements<CAP, 1, ND>(p, c, e, th_in, m_in, v_in, th_out, m_out, v_out);
+        if (blockIdx.x == 0 && e < p.n) {
+            float th[1];
+            bad |= step_elements<CAP, 1, ND>(p, c, e, th_in, m_in, v_in, th_out, m_out, v_out, th);
+        }
     }
     // overflow: warp/block OR, one atomic per block that saw a non-finite value
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
@@ -131,6 +162,8 @@ struct CommitShard {
     uint16_t* params;
     const float* master[2];
     int64_t n;
+    int8_t* qcodes;  // qwZ copy or nullptr
+    float* qscales;
 };
 
 template <int MAXS>
@@ -162,8 +195,60 @@ __device__ __forceinline__ void cast_range(const float* master, uint16_t* params
     }
 }
 
-// End of a step on the device: restore the fp16 slices if the step overflowed,
-// then the last block to finish commits or skips in the control block.
+// qwZ blocks [b0, b1) of one shard, one warp per block (warp gw of nw, in
+// grid-stride order).  With master: the fp16 values are re-cast from it and
+// written to params first (the restore of a dropped step); without: they are
+// read from params.  Then each block's scale and codes are written.  Lane l
+// holds the block's values 8l .. 8l+7; the trailing partial block is masked.
+__device__ void qwz_blocks(const float* master, uint16_t* params, int64_t n, int8_t* codes, float* scales,
+                           int64_t b0, int64_t b1, int64_t gw, int64_t nw) {
+    const int lane = threadIdx.x & 31;
+    const bool vec = ((reinterpret_cast<uintptr_t>(master) | reinterpret_cast<uintptr_t>(params)) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(codes) & 7) == 0;
+    for (int64_t b = b0 + gw; b < b1; b += nw) {
+        const int64_t e0 = b * kQwzBlock + 8 * lane;
+        const int64_t left = n - e0;
+        const int valid = left <= 0 ? 0 : (left >= 8 ? 8 : (int)left);
+        float x[8];
+        if (vec && (b + 1) * kQwzBlock <= n) {
+            if (master != nullptr) {
+                Mem<8>::load_f(master + e0, x);
+                Mem<8>::store_h(params + e0, x);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = as_fp16_value(x[j]);
+            } else {
+                Mem<8>::load_h(params + e0, x);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                x[j] = 0.0f;
+                if (j < valid) {
+                    if (master != nullptr) {
+                        const __half h = __float2half_rn(master[e0 + j]);
+                        params[e0 + j] = __half_as_ushort(h);
+                        x[j] = __half2float(h);
+                    } else {
+                        x[j] = __half2float(__ushort_as_half(params[e0 + j]));
+                    }
+                }
+            }
+        }
+        int8_t q[8];
+        const float scale = qwz_group_codes<8, 32>(x, valid, q);
+        if (vec && valid == 8) {
+            store_codes<8>(codes + e0, q);
+        } else {
+            for (int j = 0; j < valid; ++j) codes[e0 + j] = q[j];
+        }
+        if (lane == 0) scales[b] = scale;
+    }
+}
+
+// End of a step on the device: restore the fp16 slices (and their qwZ copies)
+// if the step overflowed, else write the qwZ copy of each shard's trailing
+// partial block; then the last block to finish commits or skips in the
+// control block.
 template <int MAXS>
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ CommitArgs<MAXS> p) {
     __shared__ int s_ovf, s_cur;
@@ -173,11 +258,21 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
         s_cur = *reinterpret_cast<volatile int32_t*>(&ctrl->cur);
     }
     __syncthreads();
-    if (s_ovf) {
-        const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-        for (int s = 0; s < p.n_shards; ++s)
-            cast_range(p.shards[s].master[s_cur], p.shards[s].params, p.shards[s].n, tid, stride);
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int s = 0; s < p.n_shards; ++s) {
+        const CommitShard& sh = p.shards[s];
+        const int64_t nblocks = (sh.n + kQwzBlock - 1) / kQwzBlock;
+        if (s_ovf) {
+            if (sh.qcodes != nullptr)
+                qwz_blocks(sh.master[s_cur], sh.params, sh.n, sh.qcodes, sh.qscales, 0, nblocks, tid >> 5,
+                           stride >> 5);
+            else
+                cast_range(sh.master[s_cur], sh.params, sh.n, tid, stride);
+        } else if (sh.qcodes != nullptr && sh.n % kQwzBlock != 0) {
+            qwz_blocks(nullptr, sh.params, sh.n, sh.qcodes, sh.qscales, nblocks - 1, nblocks, tid >> 5,
+                       stride >> 5);
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -203,6 +298,42 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
             c->arrivals = 0u;
             __threadfence();
         }
+    }
+}
+
+// qwZ blocks [b0, b1) on their own (see qwz_blocks).
+__global__ void __launch_bounds__(kCastThreads) qwz_kernel(const float* master, uint16_t* params, int64_t n,
+                                                           int8_t* codes, float* scales, int64_t b0, int64_t b1) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    qwz_blocks(master, params, n, codes, scales, b0, b1, tid >> 5, ((int64_t)gridDim.x * blockDim.x) >> 5);
+}
+
+// The all-gather receiver: params = fp16_rn(code * scale of its block).
+__global__ void __launch_bounds__(kCastThreads) dequant_kernel(const int8_t* codes, const float* scales, int64_t n,
+                                                               uint16_t* params) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const bool vec = ((reinterpret_cast<uintptr_t>(codes) & 7) | (reinterpret_cast<uintptr_t>(params) & 15)) == 0;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nvec = n / 8;
+        for (int64_t i = tid; i < nvec; i += stride) {
+            const uint2 w = *reinterpret_cast<const uint2*>(codes + 8 * i);
+            const float s = scales[(8 * i) / kQwzBlock];
+            float x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t word = j < 4 ? w.x : w.y;
+                const int8_t q = (int8_t)((word >> (8 * (j & 3))) & 0xffu);
+                x[j] = __fmul_rn((float)q, s);
+            }
+            Mem<8>::store_h(params + 8 * i, x);
+        }
+        done = nvec * 8;
+    }
+    for (int64_t j = done + tid; j < n; j += stride) {
+        float x[1] = {__fmul_rn((float)codes[j], scales[j / kQwzBlock])};
+        Mem<1>::store_h(params + j, x);
     }
 }
 
@@ -287,6 +418,53 @@ int32_t check_shard(const zs_shard& s, int32_t n_d, int* width) {
             else if (!zs::aligned_to(q, 32)) narrow_to(1);
         }
     }
+    if ((s.qcodes == nullptr) != (s.qscales == nullptr)) return ZS_ERR_ARG;
+    if (s.qcodes != nullptr) {
+        if (!zs::aligned_to(s.qscales, 4)) return ZS_ERR_ALIGN;
+        if (!zs::aligned_to(s.qcodes, 8)) narrow_to(0);
+        else if (!zs::aligned_to(s.qcodes, 16)) narrow_to(1);
+    }
+    return ZS_OK;
+}
+
+int32_t launch_cast(const float* master, uint16_t* params, int64_t n, cudaStream_t stream) {
+    if (n == 0) return ZS_OK;
+    const int blocks = persistent_blocks((const void*)cast_kernel, kCastThreads, (n + 7) / 8);
+    cast_kernel<<<blocks, kCastThreads, 0, stream>>>(master, params, n);
+    return zs::check_launch("cast_kernel");
+}
+
+// qwZ blocks [b0, b1) of one shard (see qwz_blocks); master != nullptr
+// re-casts the fp16 values from it first.
+int32_t launch_qwz(const float* master, uint16_t* params, int64_t n, int8_t* codes, float* scales, int64_t b0,
+                   int64_t b1, cudaStream_t stream) {
+    if (b1 <= b0) return ZS_OK;
+    const int blocks = persistent_blocks((const void*)qwz_kernel, kCastThreads, (b1 - b0) * 32);
+    qwz_kernel<<<blocks, kCastThreads, 0, stream>>>(master, params, n, codes, scales, b0, b1);
+    return zs::check_launch("qwz_kernel");
+}
+
+// After a synchronous step: the qwZ copy of every listed shard made to match
+// its fp16 slice -- on overflow the restore re-casts the slice from master[cur]
+// and re-quantizes it all (the fp16-only shards get the plain cast); else only
+// the trailing partial blocks the fused kernel left (all blocks for shards the
+// scalar kernel stepped).
+int32_t finish_sync_step(const zs_shard* shards, int32_t n_shards, const int* width, int32_t cur, bool overflow,
+                         cudaStream_t stream) {
+    for (int32_t i = 0; i < n_shards; ++i) {
+        const zs_shard& s = shards[i];
+        const int64_t nblocks = (s.n + kQwzBlock - 1) / kQwzBlock;
+        int32_t rc = ZS_OK;
+        if (overflow) {
+            if (s.qcodes != nullptr)
+                rc = launch_qwz(s.master[cur], s.params, s.n, s.qcodes, s.qscales, 0, nblocks, stream);
+            else
+                rc = launch_cast(s.master[cur], s.params, s.n, stream);
+        } else if (s.qcodes != nullptr && width[i] >= 1 && s.n % kQwzBlock != 0) {
+            rc = launch_qwz(nullptr, s.params, s.n, s.qcodes, s.qscales, nblocks - 1, nblocks, stream);
+        }
+        if (rc != ZS_OK) return rc;
+    }
     return ZS_OK;
 }
 
@@ -300,8 +478,10 @@ int32_t launch_commit_cap(const zs_shard* shards, int32_t n_shards, const zs_ada
             a.shards[i].master[0] = shards[i].master[0];
             a.shards[i].master[1] = shards[i].master[1];
             a.shards[i].n = shards[i].n;
+            a.shards[i].qcodes = shards[i].qcodes;
+            a.shards[i].qscales = shards[i].qscales;
         } else {
-            a.shards[i] = CommitShard{nullptr, {nullptr, nullptr}, 0};
+            a.shards[i] = CommitShard{nullptr, {nullptr, nullptr}, 0, nullptr, nullptr};
         }
     }
     a.n_shards = n_shards;
@@ -335,17 +515,20 @@ int32_t check_shard_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, 
 
 using zs::check_shard;
 using zs::check_shard_list;
+using zs::finish_sync_step;
+using zs::launch_cast;
+using zs::launch_qwz;
 using zs::launch_commit;
 using zs::persistent_blocks;
 using zs::valid_hp;
 
 namespace {
 
-template <int CAP, int VEC, int ND>
+template <int CAP, int VEC, int ND, bool QZ>
 int32_t launch_step_vec(const StepArgs<CAP>& a, cudaStream_t stream) {
-    const void* k = (const void*)shard_step_kernel<CAP, VEC, ND>;
+    const void* k = (const void*)shard_step_kernel<CAP, VEC, ND, QZ>;
     const int blocks = persistent_blocks(k, kThreads, a.n / VEC > 0 ? a.n / VEC : 1);
-    shard_step_kernel<CAP, VEC, ND><<<blocks, kThreads, 0, stream>>>(a);
+    shard_step_kernel<CAP, VEC, ND, QZ><<<blocks, kThreads, 0, stream>>>(a);
     return zs::check_launch("shard_step_kernel");
 }
 
@@ -369,12 +552,21 @@ int32_t launch_step_cap(const zs_shard& s, int32_t n_d, int width, const Coef* c
     a.hp = hp;
     a.ctrl = ctrl;
     a.flag = flag;
+    a.qcodes = s.qcodes;
+    a.qscales = s.qscales;
+    const bool qz = s.qcodes != nullptr;
     // the wide layout only pays once N_d > 4 (measured); scalar if misaligned
     if constexpr (ND == 0 || ND > 4) {
-        if (width == 2 && n_d > 4) return launch_step_vec<CAP, 16, ND>(a, stream);
+        if (width == 2 && n_d > 4)
+            return qz ? launch_step_vec<CAP, 16, ND, true>(a, stream) : launch_step_vec<CAP, 16, ND, false>(a, stream);
     }
-    if (width >= 1) return launch_step_vec<CAP, 8, ND>(a, stream);
-    return launch_step_vec<CAP, 1, ND>(a, stream);
+    if (width >= 1)
+        return qz ? launch_step_vec<CAP, 8, ND, true>(a, stream) : launch_step_vec<CAP, 8, ND, false>(a, stream);
+    // scalar kernel: the qwZ copy of every block follows in its own pass
+    int32_t rc = launch_step_vec<CAP, 1, ND, false>(a, stream);
+    if (rc == ZS_OK && qz)
+        rc = launch_qwz(nullptr, s.params, s.n, s.qcodes, s.qscales, 0, (s.n + kQwzBlock - 1) / kQwzBlock, stream);
+    return rc;
 }
 
 int32_t launch_step(const zs_shard& s, int32_t n_d, int width, const Coef* coef, int32_t cur,
@@ -393,13 +585,6 @@ int32_t launch_step(const zs_shard& s, int32_t n_d, int width, const Coef* coef,
     if (n_d <= 16) return launch_step_cap<16, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
     if (n_d <= 64) return launch_step_cap<64, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
     return launch_step_cap<ZS_MAX_ND, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
-}
-
-int32_t launch_cast(const float* master, uint16_t* params, int64_t n, cudaStream_t stream) {
-    if (n == 0) return ZS_OK;
-    const int blocks = persistent_blocks((const void*)cast_kernel, kCastThreads, (n + 7) / 8);
-    cast_kernel<<<blocks, kCastThreads, 0, stream>>>(master, params, n);
-    return zs::check_launch("cast_kernel");
 }
 
 }  // namespace
@@ -436,14 +621,11 @@ ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t
     err = cudaMemcpyAsync(&flag, flag_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step: read flag");
-    if (flag) {
-        for (int32_t i = 0; i < n_shards; ++i) {
-            rc = launch_cast(shards[i].master[cur], shards[i].params, shards[i].n, st);
-            if (rc != ZS_OK) return rc;
-        }
-        err = cudaStreamSynchronize(st);
-        if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step: restore");
-    }
+    // overflow: restore the fp16 slices (and qwZ copies); else finish the qwZ tails
+    rc = finish_sync_step(shards, n_shards, width, cur, flag != 0, st);
+    if (rc != ZS_OK) return rc;
+    err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step: restore");
     *overflow_out = flag ? 1 : 0;
     return ZS_OK;
 }
@@ -517,14 +699,10 @@ ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards,
     if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_noalloc: read scratch");
     int32_t flag = 0;
     for (int32_t i = 0; i < n_shards; ++i) flag |= words[i];
-    if (flag) {
-        for (int32_t i = 0; i < n_shards; ++i) {
-            rc = launch_cast(shards[i].master[cur], shards[i].params, shards[i].n, st);
-            if (rc != ZS_OK) return rc;
-        }
-        err = cudaStreamSynchronize(st);
-        if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_noalloc: restore");
-    }
+    rc = finish_sync_step(shards, n_shards, width, cur, flag != 0, st);
+    if (rc != ZS_OK) return rc;
+    err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_noalloc: restore");
     *overflow_out = flag ? 1 : 0;
     return ZS_OK;
 }
@@ -611,6 +789,11 @@ ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs
         dev.grads = mapped;
         dev.params = static_cast<uint16_t*>(mapped_host_pointer(shard->params));
         if (dev.params == nullptr) return ZS_ERR_ARG;
+        if (shard->qcodes != nullptr) {  // the qwZ copy leaves through host memory too
+            dev.qcodes = static_cast<int8_t*>(mapped_host_pointer(shard->qcodes));
+            dev.qscales = static_cast<float*>(mapped_host_pointer(shard->qscales));
+            if (dev.qcodes == nullptr || dev.qscales == nullptr) return ZS_ERR_ARG;
+        }
         // the mapping may shift addresses: recompute the access width
         rc = check_shard(dev, n_d, &width);
         if (rc != ZS_OK) return rc;
@@ -628,6 +811,26 @@ ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs
     if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_host");
     *overflow_out = flag ? 1 : 0;
     return ZS_OK;
+}
+
+ZS_API int32_t zero_qwz_quantize(const uint16_t* params_dev, int64_t n, int8_t* codes_dev, float* scales_dev,
+                                 void* stream) {
+    if (n < 0 || (n > 0 && (params_dev == nullptr || codes_dev == nullptr || scales_dev == nullptr)))
+        return ZS_ERR_ARG;
+    if (!zs::aligned_to(params_dev, 2) || !zs::aligned_to(scales_dev, 4)) return ZS_ERR_ALIGN;
+    return launch_qwz(nullptr, const_cast<uint16_t*>(params_dev), n, codes_dev, scales_dev, 0,
+                      (n + kQwzBlock - 1) / kQwzBlock, (cudaStream_t)stream);
+}
+
+ZS_API int32_t zero_qwz_dequantize(const int8_t* codes_dev, const float* scales_dev, int64_t n,
+                                   uint16_t* params_dev, void* stream) {
+    if (n < 0 || (n > 0 && (params_dev == nullptr || codes_dev == nullptr || scales_dev == nullptr)))
+        return ZS_ERR_ARG;
+    if (!zs::aligned_to(params_dev, 2) || !zs::aligned_to(scales_dev, 4)) return ZS_ERR_ALIGN;
+    if (n == 0) return ZS_OK;
+    const int blocks = persistent_blocks((const void*)dequant_kernel, kCastThreads, (n + 7) / 8);
+    dequant_kernel<<<blocks, kCastThreads, 0, (cudaStream_t)stream>>>(codes_dev, scales_dev, n, params_dev);
+    return zs::check_launch("dequant_kernel");
 }
 
 ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params_dev, int64_t n,

@@ -199,3 +199,49 @@ __device__ __forceinline__ void sum_contributions(const uint16_t* const (&grads)
     }
 }
 
+
+// ------------------------------------------------ quantized weights (qwZ) ---
+
+// Parameters per quantization block of the int8 copy of the fp16 shard.
+constexpr int kQwzBlock = ZS_QWZ_BLOCK;
+
+// One quantization block held by an aligned group of G lanes, V consecutive
+// values per lane (G * V == kQwzBlock): the block's scale max|x| / 127 and this
+// lane's V codes rint(x / scale), ties to even, all in fp32.  Lanes past the
+// data pass valid = 0.  Every lane of the warp must call it (it shuffles).
+template <int V, int G>
+__device__ __forceinline__ float qwz_group_codes(const float* x, int valid, int8_t* q) {
+    static_assert(V * G == kQwzBlock, "a group holds one block");
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+        if (j < valid) amax = fmaxf(amax, fabsf(x[j]));
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        float r = scale > 0.0f ? rintf(__fdiv_rn(x[j], scale)) : 0.0f;
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        q[j] = (int8_t)(int)r;
+    }
+    return scale;
+}
+
+// Packs V int8 codes (V = 8 or 16) and stores them with one 8- or 16-byte access.
+template <int V>
+__device__ __forceinline__ void store_codes(int8_t* dst, const int8_t* q) {
+    uint32_t w[V / 4];
+#pragma unroll
+    for (int k = 0; k < V / 4; ++k)
+        w[k] = (uint32_t)(uint8_t)q[4 * k] | ((uint32_t)(uint8_t)q[4 * k + 1] << 8) |
+               ((uint32_t)(uint8_t)q[4 * k + 2] << 16) | ((uint32_t)(uint8_t)q[4 * k + 3] << 24);
+    if constexpr (V == 8) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// fp16 rounding of a float, back in float: the value the fp16 shard holds.
+__device__ __forceinline__ float as_fp16_value(float x) { return __half2float(__float2half_rn(x)); }

@@ -38,6 +38,10 @@ bool valid_hp(const zs_adam* hp);
 // (2 = 16 elements per thread, 1 = 8, 0 = scalar).
 int32_t check_shard(const zs_shard& s, int32_t n_d, int* width);
 int32_t check_shard_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, int* width);
+// Enqueues the qwZ copy of blocks [b0, b1) of one shard (re-cast from master
+// first when master != nullptr).
+int32_t launch_qwz(const float* master, uint16_t* params, int64_t n, int8_t* codes, float* scales, int64_t b0,
+                   int64_t b1, cudaStream_t stream);
 // Enqueues the device-side commit / skip of a step over `shards`.
 int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
                       cudaStream_t stream);

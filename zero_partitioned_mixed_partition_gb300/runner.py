@@ -62,6 +62,23 @@ class WorkloadRunner:
         self.ctrl = binding.new_ctrl(self.device)
         binding.zero_ctrl_init(self.ctrl, w.loss_scale, stream=self.stream)
 
+    def enable_qwz(self):
+        """Give every stepped shard an int8 qwZ copy of its fp16 slice (codes
+        and per-256 scales) that each step keeps in sync, and quantize the
+        initial slice."""
+        self.qwz = {}
+        views = []
+        for view, r in zip(self.views, self.shard_ids):
+            n = self.n_valid[r]
+            codes = torch.zeros(self.S, dtype=torch.int8, device=self.device)
+            scales = torch.zeros((self.S + binding.ZS_QWZ_BLOCK - 1) // binding.ZS_QWZ_BLOCK, dtype=torch.float32,
+                                 device=self.device)
+            master, m, v, params = self.state[r]
+            views.append(binding.ShardView(self.grads[r], master, m, v, params, n, qcodes=codes, qscales=scales))
+            binding.zero_qwz_quantize(params, n, codes, scales, stream=self.stream)
+            self.qwz[r] = (codes, scales)
+        self.views = views
+
     # ---------------------------------------------------------------- steps --
     def step(self):
         """One whole step over every stepped shard, stream-ordered."""
@@ -108,6 +125,34 @@ class WorkloadRunner:
         cur = self.ctrl_host()["cur"]
         master, m, v, params = self.state[r]
         return master[cur], m[cur], v[cur], params
+
+    # ------------------------------------------------------- checkpointing --
+    def save(self) -> dict:
+        """Host copy of everything a resumed run needs: the control block's
+        bytes (loss scale, t, beta^t, ping-pong set, counters) and, per shard,
+        the committed master/m/v and the fp16 slice.  Call with the stream idle."""
+        torch.cuda.synchronize(self.device)
+        cur = self.ctrl_host()["cur"]
+        out = {"ctrl": self.ctrl.detach().cpu().clone(), "shards": {}}
+        for r in self.shard_ids:
+            master, m, v, params = self.state[r]
+            out["shards"][r] = tuple(t.detach().cpu().clone() for t in (master[cur], m[cur], v[cur], params))
+        return out
+
+    def load(self, ckpt: dict):
+        """Restore a save() of a runner of the same workload: the state goes
+        into the set the saved control block names, the control block is
+        copied back as bytes."""
+        ctrl = ckpt["ctrl"]
+        self.ctrl.copy_(ctrl.to(self.device))
+        cur = binding.read_ctrl(self.ctrl)["cur"]
+        for r, (master, m, v, params) in ckpt["shards"].items():
+            dm, dmm, dv, dp = self.state[r]
+            dm[cur].copy_(master.to(self.device))
+            dmm[cur].copy_(m.to(self.device))
+            dv[cur].copy_(v.to(self.device))
+            dp.copy_(params.to(self.device))
+        torch.cuda.synchronize(self.device)
 
     # ------------------------------------------------------------ accounting --
     def bytes_per_step(self) -> int:
