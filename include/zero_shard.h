@@ -335,6 +335,20 @@ ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params
                                        void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* The step on the host CPU cores (ZeRO-Offload, "DeepSpeed ZeRO Stages",     */
+/* sec. 5.1: optimizer state and update on the CPU, with SIMD and threads).  */
+/* ------------------------------------------------------------------------ */
+
+/* zero_shard_step with every buffer in HOST memory (grads[k], master, m, v,
+ * params; no qwZ copy), run on n_threads host threads (0 = all cores).  Same
+ * arithmetic, ping-pong, overflow test and restore as zero_shard_step, bit for
+ * bit; synchronous; *overflow_out (HOST) gets 0 or 1 and the caller commits as
+ * for zero_shard_step.  No CUDA call. */
+ZS_API int32_t zero_shard_step_cpu(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                   const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
+                                   int32_t n_threads, int32_t* overflow_out);
+
+/* ------------------------------------------------------------------------ */
 /* Quantized weights (qwZ) on their own.                                     */
 /* ------------------------------------------------------------------------ */
 

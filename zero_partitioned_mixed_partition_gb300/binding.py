@@ -80,6 +80,7 @@ _SIGNATURES = {
     "zero_shard_step_clipped_async": (_I32, [_P, _I32, _I32, _P, _F64, _P, _P, _P, _P]),
     "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
+    "zero_shard_step_cpu": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _I32, _P]),
     "zero_qwz_quantize": (_I32, [_P, _I64, _P, _P, _P]),
     "zero_qwz_dequantize": (_I32, [_P, _P, _I64, _P, _P]),
     "zero_status_string": (ctypes.c_char_p, [_I32]),
@@ -324,6 +325,42 @@ class HostShardView(ShardView):
                     raise TypeError("host shard: qwZ buffers must be pinned host tensors")
             self.struct.qcodes = qcodes.data_ptr()
             self.struct.qscales = qscales.data_ptr()
+
+
+class CpuShardView(ShardView):
+    """A shard whose buffers all live in host memory (CPU torch tensors), for
+    the step on the host cores."""
+
+    def __init__(self, grads, master, m, v, params, n):
+        def host(t, dtype, what):
+            if t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+                raise TypeError(f"{what}: expected a contiguous host {dtype} tensor")
+            return t.data_ptr()
+        self.grads = list(grads)
+        self.master, self.m, self.v = tuple(master), tuple(m), tuple(v)
+        self.params = params
+        self.n = int(n)
+        self._table = (_P * max(len(self.grads), 1))(*[host(g, torch.float16, "grads") for g in self.grads])
+        self.struct = Shard()
+        self.struct.grads = ctypes.cast(self._table, ctypes.POINTER(_P))
+        for i in range(2):
+            self.struct.master[i] = host(self.master[i], torch.float32, "master")
+            self.struct.m[i] = host(self.m[i], torch.float32, "m")
+            self.struct.v[i] = host(self.v[i], torch.float32, "v")
+        self.struct.params = host(params, torch.float16, "params")
+        self.struct.n = self.n
+
+
+def zero_shard_step_cpu(shards: Sequence[ShardView], n_d: int, hp: Adam, loss_scale: float, step: int, cur: int,
+                        n_threads: int = 0) -> int:
+    """The shard step on the host cores (every buffer in host memory); returns
+    the overflow flag.  Same results as zero_shard_step, bit for bit."""
+    arr = _shard_array(shards)
+    ovf = _I32(-1)
+    rc = lib().zero_shard_step_cpu(arr, len(shards), int(n_d), ctypes.byref(hp), float(loss_scale), int(step),
+                                   int(cur), int(n_threads), ctypes.byref(ovf))
+    _check(rc, "zero_shard_step_cpu")
+    return int(ovf.value)
 
 
 def zero_shard_step_host(shard: HostShardView, n_d: int, hp: Adam, ctrl_dev: torch.Tensor, stream=None) -> int:

@@ -19,12 +19,13 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libzeroshard.so")
 
-SOURCES = ["shard_step.cu", "clip.cu", "layout.cu", "diag.cpp"]
+SOURCES = ["shard_step.cu", "clip.cu", "layout.cu", "cpu_step.cpp", "diag.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-# -ffp-contract=off keeps the host-side coefficient arithmetic free of fused
-# multiply-adds, matching the device code's explicit _rn operations.
+# -ffp-contract=off keeps host arithmetic (step coefficients, the CPU step) free
+# of fused multiply-adds, matching the device code's explicit _rn operations;
+# -fno-math-errno lets the host compiler vectorise sqrtf (results unchanged).
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
-              "-Xcompiler", "-fPIC,-fvisibility=hidden,-ffp-contract=off",
+              "-Xcompiler", "-O3,-fPIC,-fvisibility=hidden,-ffp-contract=off,-fno-math-errno",
               "-I", INCLUDE, "-I", CSRC]
 
 
