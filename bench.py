@@ -194,6 +194,32 @@ def oracle_throughput(w, n_sample: int, seconds: float, threads: int):
     return n_sample * steps / el / 1e9, steps, el, threads
 
 
+def native_cpu_throughput(w, n_sample: int, seconds: float, threads: int):
+    """The library's own CPU step (zero_shard_step_cpu: the ZeRO-Offload
+    optimizer on the host cores) on a bounded sample of the workload.
+    Returns (Gparams/s, steps, seconds, threads)."""
+    import torch
+    from zero_partitioned_mixed_partition_gb300 import binding, synth
+    grads = [synth.grad_contribution(w, n_sample, k, 1, shard=w.rank or 0) for k in range(w.n_d)]
+    master = (synth.master_init(w, n_sample, shard=w.rank or 0), torch.zeros(n_sample))
+    m = (torch.zeros(n_sample), torch.zeros(n_sample))
+    v = (torch.zeros(n_sample), torch.zeros(n_sample))
+    params = torch.zeros(n_sample, dtype=torch.float16)
+    view = binding.CpuShardView(grads, master, m, v, params, n_sample)
+    hp = binding.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    binding.zero_shard_step_cpu([view], w.n_d, hp, w.loss_scale, 1, 0, n_threads=threads)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        ovf = binding.zero_shard_step_cpu([view], w.n_d, hp, w.loss_scale, steps + 2, (steps + 1) % 2,
+                                          n_threads=threads)
+        assert ovf == 0
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return n_sample * steps / el / 1e9, steps, el, threads
+
+
 def reference_arm(args, rank: int):
     """The oracle timed on the host cores as the reference arm."""
     if rank != 0:
@@ -414,6 +440,12 @@ def main():
         line["cpu_baseline"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th, "kind": "oracle",
                                 "sample": f"{min(4_000_000, elems):,} params of the shard x N_d={w.n_d}, "
                                           f"{steps} steps in {el:.1f} s over {th} threads"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ns = min(32_000_000, elems)
+        g, steps, el, th = native_cpu_throughput(w, ns, 3.0, os.cpu_count() or 1)
+        line["cpu_native"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th,
+                              "kind": "zero_shard_step_cpu (ZeRO-Offload step on the host cores)",
+                              "sample": f"{ns:,} params x N_d={w.n_d}, {steps} steps in {el:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
