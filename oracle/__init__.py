@@ -84,6 +84,8 @@ def _load():
             lib.oracle_clip_factor.restype = ctypes.c_float
             lib.oracle_scale.argtypes = [_P, _I64, ctypes.c_float]
             lib.oracle_scale.restype = None
+            lib.oracle_sgd_apply.argtypes = [_P, _I64, _P, _P, _P, _F64, _F64, _F64]
+            lib.oracle_sgd_apply.restype = _I32
             lib.oracle_qwz_quantize.argtypes = [_P, _I64, _P, _P]
             lib.oracle_qwz_quantize.restype = None
             lib.oracle_qwz_dequantize.argtypes = [_P, _P, _I64, _P]
@@ -260,3 +262,18 @@ def qwz_dequantize(codes, scales):
     out = np.empty(c.size, np.uint16)
     _load().oracle_qwz_dequantize(_ptr(c), _ptr(s), c.size, _ptr(out))
     return out
+
+
+# ----------------------------------------------------- SGD with momentum ---
+
+def sgd_apply(g, master, mom, params, *, lr, momentum, weight_decay):
+    """In-place SGD-with-momentum update of float32 master / momentum and
+    uint16 params."""
+    g = _contig(g, np.float32)
+    for a in (master, mom):
+        if a.dtype != np.float32 or not a.flags.c_contiguous:
+            raise TypeError("state arrays must be contiguous float32")
+    rc = _load().oracle_sgd_apply(_ptr(g), g.size, _ptr(master), _ptr(mom), _ptr(params), lr, momentum,
+                                  weight_decay)
+    if rc != 0:
+        raise ValueError("oracle_sgd_apply: invalid arguments")

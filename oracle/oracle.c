@@ -31,6 +31,9 @@
  *   oracle_clip_factor,  the reduced gradient, the clip factor and the
  *   oracle_scale         scaled gradient ("DeepSpeed ZeRO Stages" sec. 2.1,
  *                        Fact 1: clipping needs ||g||_2 over all of P)
+ *   oracle_sgd_apply     mixed-precision SGD with momentum on the shard, the
+ *                        other optimizer the state multiplier K names
+ *                        ("DeepSpeed ZeRO Stages" sec. 1.2)
  *   oracle_qwz_quantize, block-wise int8 quantization of the fp16 shard for
  *   oracle_qwz_dequantize the parameter all-gather and its inverse
  *                        ("ZeRO Optimization: Stages 1, 2, and 3 Explained",
@@ -59,6 +62,9 @@
  *     shard of the reduced, unscaled gradient, summed in double;
  *     c = min(1, max_norm / (||g||_2 + 1e-6)) in double, rounded once to
  *     float, and g' = g * c in fp32 before the Adam update;
+ *   - SGD with momentum (named with its K, no formula): the textbook rule,
+ *     d = g + wd theta, b' = mu b + d (b = 0 before the first step),
+ *     theta' = theta - lr b', fp32 master and fp32 momentum;
  *   - quantized weights (the pages give blocks with their own scale, 16 -> 8
  *     bit, nothing more): blocks of 256 consecutive parameters of the shard,
  *     the last one possibly shorter; scale = max|x| / 127 in fp32;
@@ -409,4 +415,32 @@ void oracle_qwz_dequantize(const int8_t* codes, const float* scales, int64_t n, 
 {
     for (int64_t j = 0; j < n; ++j)
         params[j] = oracle_f32_to_f16((float)codes[j] * scales[j / ORACLE_QWZ_BLOCK]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* SGD with momentum.                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Mixed-precision SGD with momentum on n coordinates, in place on the fp32
+ * master theta and momentum b, writing fp16(theta') into params:
+ *   d  = g + wd theta          (L2 weight decay folded into the gradient)
+ *   b' = mu b + d              (b starts at 0)
+ *   th'= theta - lr b'
+ * The pages name this optimizer through its state multiplier K ("DeepSpeed
+ * ZeRO Stages" sec. 1.2) and give no formula; this is the textbook rule. */
+int32_t oracle_sgd_apply(const float* g, int64_t n, float* master, float* mom, uint16_t* params,
+                         double lr, double momentum, double weight_decay)
+{
+    if (n < 0 || (n > 0 && (g == NULL || master == NULL || mom == NULL))) return ORACLE_ERR_ARG;
+    float lr_f = (float)lr, mu = (float)momentum, wd_f = (float)weight_decay;
+    for (int64_t j = 0; j < n; ++j) {
+        float th = master[j];
+        float d = g[j] + wd_f * th;
+        float b = mu * mom[j] + d;
+        float th_new = th - lr_f * b;
+        mom[j] = b;
+        master[j] = th_new;
+        if (params) params[j] = oracle_f32_to_f16(th_new);
+    }
+    return ORACLE_OK;
 }
