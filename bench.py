@@ -50,6 +50,8 @@ def parse_args():
                     help="global gradient-norm clipping at this max norm (two-pass step); 0 = off")
     ap.add_argument("--clip-keep-g", action="store_true",
                     help="with --clip: pass 1 keeps the fp32 reduced gradient for pass 2")
+    ap.add_argument("--optimizer", default="adam", choices=["adam", "sgd"],
+                    help="adam (the pages' mixed-precision Adam) or sgd (SGD with momentum 0.9)")
     ap.add_argument("--qwz", action="store_true",
                     help="keep the int8 qwZ copy of the fp16 shard in each step (1 + 4/256 bytes per element)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -297,6 +299,9 @@ def main():
     torch.cuda.synchronize()
 
     clip = args.clip > 0
+    sgd_hp = binding.sgd(w.lr, 0.9, w.weight_decay)
+    if args.optimizer == "sgd" and (clip or args.qwz):
+        raise SystemExit("--optimizer sgd goes without --clip / --qwz")
     if clip:
         run.enable_clipping(args.clip_keep_g)
     if args.qwz:
@@ -305,6 +310,13 @@ def main():
     def one_step(ev=None):
         binding.zero_partition_layout_device(numels_dev, w.n_d, w.align, lay_scalars, lay_toff, lay_soff,
                                              lay_frags, cap, stream=stream)
+        if args.optimizer == "sgd":
+            if ev is not None:
+                ev[0].record(stream)
+            run.step_sgd(sgd_hp)  # fused kernel(s) and the commit
+            if ev is not None:
+                ev[1].record(stream)
+            return
         if not clip:
             if ev is not None:
                 ev[0].record(stream)
@@ -374,6 +386,8 @@ def main():
     total_elems = elems * world
     value = total_elems * args.steps / (ms_max / 1e3) / 1e9
     bytes_step = run.clipped_bytes_per_step() if clip else run.bytes_per_step()
+    if args.optimizer == "sgd":  # fp32 master + momentum: 2 N_d + 18 bytes per element
+        bytes_step = sum((2 * w.n_d + 18) * run.n_valid[r] for r in run.shard_ids)
     if args.qwz:  # int8 codes + one fp32 scale per 256 elements, written by the step
         bytes_step += sum(run.n_valid[r] + 4 * ((run.n_valid[r] + 255) // 256) for r in run.shard_ids)
     hbm_gbs = bytes_step * world * args.steps / (ms_max / 1e3) / 1e9
@@ -385,7 +399,7 @@ def main():
     traffic_per_param = recorded_traffic(os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc",
                                                       "shard_step.cu"))
     traffic = None
-    if traffic_per_param and w.n_d in traffic_per_param and not clip and not args.qwz:
+    if traffic_per_param and w.n_d in traffic_per_param and not clip and not args.qwz and args.optimizer == "adam":
         traffic = round(traffic_per_param[w.n_d] * elems)
     clip_info = None
     if clip:
@@ -430,6 +444,9 @@ def main():
         "gpu_launches": int(launches),
         "e2e": e2e,
     }
+    if args.optimizer == "sgd":
+        line["optimizer"] = {"kind": "sgd", "momentum": 0.9, "timed": "fused kernel + commit"}
+        line["roofline"]["kernel"] = "sgd_step_kernel + commit_kernel"
     if args.qwz:
         line["qwz"] = {"block": 256, "extra_bytes_per_param": round(1 + 4 / 256, 4)}
     if clip_info is not None:

@@ -81,6 +81,13 @@ typedef struct zs_adam {
     double weight_decay;
 } zs_adam;
 
+/* SGD-with-momentum hyper-parameters (zero_shard_step_sgd_async). */
+typedef struct zs_sgd {
+    double lr;
+    double momentum;      /* mu >= 0; 0 gives plain SGD */
+    double weight_decay;  /* L2 decay folded into the gradient */
+} zs_sgd;
+
 /* One shard of the optimizer state, as one rank owns it.
  *   grads     HOST array of n_d DEVICE pointers; grads[k] is simulated rank
  *             k's fp16 gradient for the elements of this shard (scaled by the
@@ -333,6 +340,21 @@ ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_s
  * fp16 parameter slice from fp32 master weights.  Stream-ordered. */
 ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params_dev, int64_t n,
                                        void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Mixed-precision SGD with momentum (the other optimizer of the state        */
+/* multiplier K, "DeepSpeed ZeRO Stages", sec. 1.2).                         */
+/* ------------------------------------------------------------------------ */
+
+/* The step of zero_shard_step_async with SGD with momentum in place of Adam:
+ *   g as for Adam,  d = g + weight_decay theta,  b' = momentum b + d,
+ *   theta' = theta - lr b',  params = fp16_rn(theta')
+ * The momentum b lives in zs_shard.m (both sets; b starts at 0), zs_shard.v
+ * is unused (may be NULL) and qcodes must be NULL.  Loss scale and the
+ * ping-pong set come from *ctrl_dev; one fused kernel per shard, then the
+ * device commit.  Per element 2 n_d + 18 bytes. */
+ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                         const zs_sgd* hp, zs_ctrl* ctrl_dev, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* The step on the host CPU cores (ZeRO-Offload, "DeepSpeed ZeRO Stages",     */

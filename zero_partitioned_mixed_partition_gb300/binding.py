@@ -51,6 +51,10 @@ class Shard(ctypes.Structure):
                 ("params", _P), ("n", _I64), ("qcodes", _P), ("qscales", _P)]
 
 
+class Sgd(ctypes.Structure):
+    _fields_ = [("lr", _F64), ("momentum", _F64), ("weight_decay", _F64)]
+
+
 class Ctrl(ctypes.Structure):
     _fields_ = [("loss_scale", _F64), ("beta1_pow", _F64), ("beta2_pow", _F64), ("step", _I64),
                 ("skipped", _I64), ("cur", _I32), ("overflow", _I32), ("last_overflow", _I32),
@@ -81,6 +85,7 @@ _SIGNATURES = {
     "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
     "zero_shard_step_cpu": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _I32, _P]),
+    "zero_shard_step_sgd_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "zero_qwz_quantize": (_I32, [_P, _I64, _P, _P, _P]),
     "zero_qwz_dequantize": (_I32, [_P, _P, _I64, _P, _P]),
     "zero_status_string": (ctypes.c_char_p, [_I32]),
@@ -251,6 +256,18 @@ def _shard_array(shards: Sequence[ShardView]):
 def adam(lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
          weight_decay: float = 0.0) -> Adam:
     return Adam(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay))
+
+
+def sgd(lr: float, momentum: float = 0.9, weight_decay: float = 0.0) -> Sgd:
+    return Sgd(float(lr), float(momentum), float(weight_decay))
+
+
+def zero_shard_step_sgd_async(shards: Sequence[ShardView], n_d: int, hp: Sgd, ctrl_dev: torch.Tensor, stream=None):
+    """Stream-ordered step with SGD with momentum (momentum in ShardView.m)."""
+    arr = _shard_array(shards)
+    rc = lib().zero_shard_step_sgd_async(arr, len(shards), int(n_d), ctypes.byref(hp),
+                                         _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_step_sgd_async")
 
 
 def zero_shard_step(shards: Sequence[ShardView], n_d: int, hp: Adam, loss_scale: float, step: int, cur: int,

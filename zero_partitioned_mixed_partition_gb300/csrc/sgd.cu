@@ -1,0 +1,203 @@
+// sgd.cu -- the shard step with mixed-precision SGD with momentum.
+//
+// The other optimizer the pages name through its state multiplier K
+// ("DeepSpeed ZeRO Stages", sec. 1.2).  Same structure as the Adam step: the
+// N_d fp16 contributions are summed in rank order in fp32, averaged and
+// unscaled, tested for non-finite values, and the update
+//   d = g + wd theta,  b' = mu b + d,  theta' = theta - lr b'
+// runs on the fp32 master and momentum (ping-pong, read set cur, write cur ^ 1)
+// with the fp16 cast, every fp32 operation rounded once.  The device commit
+// of the Adam step is reused (its beta^t bookkeeping is unused here).
+// Per element: 2 N_d + 8 bytes read, 8 + 2 written.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "zs_internal.h"
+
+namespace {
+
+#include "step_common.cuh"
+
+// Threads per block: 512 for the 16-element layout with 32 or more
+// contributions (CAP >= 32), which at its ~80 registers puts exactly one block
+// (512 threads) on each SM -- measured on the N_d = 64 shard: 7.13 TB/s
+// against 5.97 TB/s for three 256-thread blocks per SM; 256 otherwise (at
+// N_d = 16 the 512-thread block was 2.6 % slower).  A persistent grid must
+// also fill the SMs' capacity exactly: capping it below lets the scheduler
+// stack blocks on some SMs and leave others idle (4.65 TB/s).
+template <int VEC, int CAP>
+constexpr int sgd_threads() { return (VEC == 16 && CAP >= 32) ? 512 : 256; }
+
+template <int CAP>
+struct SgdArgs {
+    const uint16_t* grads[CAP];
+    float* master[2];
+    float* mom[2];
+    uint16_t* params;
+    int64_t n;
+    int32_t n_d;
+    double lr, momentum, weight_decay;
+    const zs_ctrl* ctrl;  // loss scale and the ping-pong set
+    int32_t* flag;        // &ctrl->overflow
+};
+
+template <int CAP, int VEC, int ND>
+__device__ __forceinline__ uint32_t sgd_elements(const SgdArgs<CAP>& p, float inv, float lr, float mu, float wd,
+                                                 int64_t e, const float* th_in, const float* b_in,
+                                                 float* th_out, float* b_out) {
+    float th[VEC], b[VEC], acc[VEC];
+    Mem<VEC>::load_f(th_in + e, th);
+    Mem<VEC>::load_f(b_in + e, b);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
+    sum_contributions<CAP, VEC, ND>(p.grads, p.n_d, e, acc);
+    uint32_t bad = 0;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        bad |= nonfinite(acc[j]) ? 1u : 0u;
+        const float g = __fmul_rn(acc[j], inv);
+        const float d = __fadd_rn(g, __fmul_rn(wd, th[j]));
+        b[j] = __fadd_rn(__fmul_rn(mu, b[j]), d);
+        th[j] = __fsub_rn(th[j], __fmul_rn(lr, b[j]));
+    }
+    Mem<VEC>::store_f(th_out + e, th);
+    Mem<VEC>::store_f(b_out + e, b);
+    Mem<VEC>::store_h(p.params + e, th);
+    return bad;
+}
+
+template <int CAP, int VEC, int ND>
+__global__ void __launch_bounds__(sgd_threads<VEC, CAP>()) sgd_step_kernel(const __grid_constant__ SgdArgs<CAP> p) {
+    __shared__ float s_inv;
+    __shared__ int s_cur;
+    if (threadIdx.x == 0) {
+        s_inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)p.n_d, p.ctrl->loss_scale)));
+        s_cur = p.ctrl->cur;
+    }
+    __syncthreads();
+    const float inv = s_inv;
+    const int cur = s_cur;
+    const float lr = __double2float_rn(p.lr), mu = __double2float_rn(p.momentum), wd = __double2float_rn(p.weight_decay);
+    const float* th_in = p.master[cur];
+    const float* b_in = p.mom[cur];
+    float* th_out = p.master[cur ^ 1];
+    float* b_out = p.mom[cur ^ 1];
+    uint32_t bad = 0;
+    const int64_t nvec = p.n / VEC;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
+        bad |= sgd_elements<CAP, VEC, ND>(p, inv, lr, mu, wd, i * VEC, th_in, b_in, th_out, b_out);
+    if (VEC > 1) {
+        const int64_t e = nvec * VEC + threadIdx.x;
+        if (blockIdx.x == 0 && e < p.n) bad |= sgd_elements<CAP, 1, ND>(p, inv, lr, mu, wd, e, th_in, b_in, th_out, b_out);
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
+}
+
+template <int CAP, int VEC, int ND>
+int32_t launch_vec(const SgdArgs<CAP>& a, cudaStream_t stream) {
+    const void* k = (const void*)sgd_step_kernel<CAP, VEC, ND>;
+    constexpr int threads = sgd_threads<VEC, CAP>();
+    const int blocks = zs::persistent_blocks(k, threads, a.n / VEC > 0 ? a.n / VEC : 1);
+    sgd_step_kernel<CAP, VEC, ND><<<blocks, threads, 0, stream>>>(a);
+    return zs::check_launch("sgd_step_kernel");
+}
+
+template <int CAP, int ND>
+int32_t launch_cap(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl,
+                   cudaStream_t stream) {
+    SgdArgs<CAP> a;
+    for (int k = 0; k < CAP; ++k) a.grads[k] = k < n_d ? s.grads[k] : nullptr;
+    for (int i = 0; i < 2; ++i) {
+        a.master[i] = s.master[i];
+        a.mom[i] = s.m[i];
+    }
+    a.params = s.params;
+    a.n = s.n;
+    a.n_d = n_d;
+    a.lr = hp.lr;
+    a.momentum = hp.momentum;
+    a.weight_decay = hp.weight_decay;
+    a.ctrl = ctrl;
+    a.flag = &ctrl->overflow;
+    if constexpr (ND == 0 || ND > 4) {
+        if (width == 2 && n_d > 4) return launch_vec<CAP, 16, ND>(a, stream);
+    }
+    if (width >= 1) return launch_vec<CAP, 8, ND>(a, stream);
+    return launch_vec<CAP, 1, ND>(a, stream);
+}
+
+int32_t launch(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+    switch (n_d) {
+    case 16: return launch_cap<16, 16>(s, n_d, width, hp, ctrl, stream);
+    case 32: return launch_cap<32, 32>(s, n_d, width, hp, ctrl, stream);
+    case 64: return launch_cap<64, 64>(s, n_d, width, hp, ctrl, stream);
+    default: break;
+    }
+    if (n_d <= 4) return launch_cap<4, 0>(s, n_d, width, hp, ctrl, stream);
+    if (n_d <= 16) return launch_cap<16, 0>(s, n_d, width, hp, ctrl, stream);
+    if (n_d <= 64) return launch_cap<64, 0>(s, n_d, width, hp, ctrl, stream);
+    return launch_cap<ZS_MAX_ND, 0>(s, n_d, width, hp, ctrl, stream);
+}
+
+// Checks one SGD shard (v unused, no qwZ copy); *width as for the Adam step.
+int32_t check_sgd_shard(const zs_shard& s, int32_t n_d, int* width) {
+    if (s.n < 0) return ZS_ERR_ARG;
+    if (s.qcodes != nullptr || s.qscales != nullptr) return ZS_ERR_ARG;
+    *width = 2;
+    if (s.n == 0) return ZS_OK;
+    if (s.grads == nullptr || s.params == nullptr) return ZS_ERR_ARG;
+    auto narrow_to = [width](int w) { if (w < *width) *width = w; };
+    for (int k = 0; k < n_d; ++k) {
+        if (s.grads[k] == nullptr) return ZS_ERR_ARG;
+        if (!zs::aligned_to(s.grads[k], 2)) return ZS_ERR_ALIGN;
+        if (!zs::aligned_to(s.grads[k], 16)) narrow_to(0);
+    }
+    if (!zs::aligned_to(s.params, 2)) return ZS_ERR_ALIGN;
+    if (!zs::aligned_to(s.params, 16)) narrow_to(0);
+    for (int i = 0; i < 2; ++i) {
+        const void* st[] = {s.master[i], s.m[i]};
+        for (const void* q : st) {
+            if (q == nullptr) return ZS_ERR_ARG;
+            if (!zs::aligned_to(q, 4)) return ZS_ERR_ALIGN;
+            if (!zs::aligned_to(q, 16)) narrow_to(0);
+            else if (!zs::aligned_to(q, 32)) narrow_to(1);
+        }
+    }
+    return ZS_OK;
+}
+
+bool valid_sgd(const zs_sgd* hp) {
+    if (hp == nullptr) return false;
+    const double v[] = {hp->lr, hp->momentum, hp->weight_decay};
+    for (double x : v)
+        if (!(x == x) || x > 1e300 || x < -1e300) return false;
+    return hp->momentum >= 0.0;
+}
+
+}  // namespace
+
+extern "C" {
+
+ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shards, int32_t n_d, const zs_sgd* hp,
+                                         zs_ctrl* ctrl_dev, void* stream) {
+    if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS || n_d < 1 || n_d > ZS_MAX_ND ||
+        !valid_sgd(hp) || ctrl_dev == nullptr)
+        return ZS_ERR_ARG;
+    if (!zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
+    int width[ZS_MAX_SHARDS];
+    for (int32_t i = 0; i < n_shards; ++i) {
+        int32_t rc = check_sgd_shard(shards[i], n_d, &width[i]);
+        if (rc != ZS_OK) return rc;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int32_t i = 0; i < n_shards; ++i) {
+        if (shards[i].n == 0) continue;
+        int32_t rc = launch(shards[i], n_d, width[i], *hp, ctrl_dev, st);
+        if (rc != ZS_OK) return rc;
+    }
+    const zs_adam no_adam{hp->lr, 0.0, 0.0, 0.0, 0.0};  // the commit's beta^t are unused by SGD
+    return zs::launch_commit(shards, n_shards, no_adam, ctrl_dev, st);
+}
+
+}  // extern "C"

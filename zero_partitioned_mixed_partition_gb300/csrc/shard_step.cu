@@ -364,7 +364,7 @@ namespace zs {
 
 // Persistent grid: enough blocks to fill every SM at the kernel's occupancy,
 // never more than the work needs.
-int persistent_blocks(const void* kernel, int threads, int64_t work_items) {
+int persistent_blocks(const void* kernel, int threads, int64_t work_items, int max_per_sm) {
     static std::mutex mu;
     static std::unordered_map<const void*, int> per_sm;
     int bps = 0;
@@ -379,6 +379,7 @@ int persistent_blocks(const void* kernel, int threads, int64_t work_items) {
         std::lock_guard<std::mutex> lock(mu);
         per_sm[kernel] = bps;
     }
+    if (max_per_sm > 0 && bps > max_per_sm) bps = max_per_sm;
     const int64_t full = (int64_t)bps * zs::device_sm_count();
     const int64_t need = (work_items + threads - 1) / threads;
     int64_t blocks = need < full ? need : full;

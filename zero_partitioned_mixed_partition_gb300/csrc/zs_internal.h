@@ -29,9 +29,10 @@ inline int32_t check_launch(const char* where, int64_t n = 1) {
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
-// Persistent grid for `kernel`: every SM filled at the kernel's occupancy, no
-// more blocks than work_items / threads.
-int persistent_blocks(const void* kernel, int threads, int64_t work_items);
+// Persistent grid for `kernel`: every SM filled at the kernel's occupancy
+// (at most max_per_sm blocks per SM when > 0), no more blocks than
+// work_items / threads.
+int persistent_blocks(const void* kernel, int threads, int64_t work_items, int max_per_sm = 0);
 // Hyper-parameters finite, betas in [0, 1), eps >= 0.
 bool valid_hp(const zs_adam* hp);
 // Checks one shard's pointers; *width gets the access width they allow

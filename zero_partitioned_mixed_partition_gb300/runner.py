@@ -84,6 +84,10 @@ class WorkloadRunner:
         """One whole step over every stepped shard, stream-ordered."""
         binding.zero_shard_step_async(self.views, self.w.n_d, self.hp, self.ctrl, stream=self.stream)
 
+    def step_sgd(self, hp):
+        """One step with SGD with momentum (momentum kept in the m buffers)."""
+        binding.zero_shard_step_sgd_async(self.views, self.w.n_d, hp, self.ctrl, stream=self.stream)
+
     def reduce_adam(self, i: int = 0):
         binding.zero_shard_reduce_adam_async(self.views[i], self.w.n_d, self.hp, self.ctrl, stream=self.stream)
 
