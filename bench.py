@@ -54,6 +54,8 @@ def parse_args():
                     help="adam (the pages' mixed-precision Adam) or sgd (SGD with momentum 0.9)")
     ap.add_argument("--qwz", action="store_true",
                     help="keep the int8 qwZ copy of the fp16 shard in each step (1 + 4/256 bytes per element)")
+    ap.add_argument("--log-steps", default="",
+                    help="write one JSON record per timed step (kernel ms, rank, workload) to this file")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-mode", default="mapped", choices=["mapped", "staged"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -379,6 +381,15 @@ def main():
         norm_ms = [ev[0].elapsed_time(ev[2]) for ev in pairs]
         upd_ms = [ev[2].elapsed_time(ev[1]) for ev in pairs]
     ctrl = run.ctrl_host()
+    if args.log_steps:
+        path = args.log_steps if world == 1 else f"{args.log_steps}.rank{rank}"
+        bps = run.clipped_bytes_per_step() if clip else run.bytes_per_step()
+        with open(path, "w") as f:
+            for k, (ev, ms) in enumerate(zip(pairs, kern_ms)):
+                f.write(json.dumps({"rank": rank, "workload": w.name, "timed_step": k, "kernel_ms": round(ms, 5),
+                                    "kernel_gbs": round(bps / (ms / 1e3) / 1e9, 1),
+                                    "gparams_s": round(run.elements_per_step() / (ms / 1e3) / 1e9, 3)}) + "\n")
+            f.write(json.dumps({"rank": rank, "final_ctrl": ctrl}) + "\n")
     assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + args.warmup + args.steps, ctrl
 
     ms_max = zdist.max_over_ranks(ms_total, device=dev)

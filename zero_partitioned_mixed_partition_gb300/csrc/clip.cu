@@ -299,6 +299,7 @@ ZS_API int32_t zero_shard_clipped_adam_async(const zs_shard* shard, int32_t n_d,
 ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                              const zs_adam* hp, double max_norm, float* const* g_dev,
                                              double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream) {
+    zs::NvtxRange nvtx_range("zero_shard_step_clipped_async");
     if (n_d < 1 || n_d > ZS_MAX_ND || !zs::valid_hp(hp) || sqnorm_dev == nullptr || ctrl_dev == nullptr ||
         !(max_norm == max_norm))
         return ZS_ERR_ARG;

@@ -121,6 +121,7 @@ extern "C" {
 ZS_API int32_t zero_shard_step_cpu(const zs_shard* shards, int32_t n_shards, int32_t n_d, const zs_adam* hp,
                                    double loss_scale, int64_t step, int32_t cur, int32_t n_threads,
                                    int32_t* overflow_out) {
+    zs::NvtxRange nvtx_range("zero_shard_step_cpu");
     if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS || n_d < 1 || n_d > ZS_MAX_ND ||
         !zs::valid_hp(hp) || !(loss_scale > 0.0) || loss_scale > 1e300 || step < 1 || (cur != 0 && cur != 1) ||
         overflow_out == nullptr || n_threads < 0)

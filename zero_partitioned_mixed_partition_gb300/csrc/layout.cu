@@ -179,6 +179,7 @@ ZS_API int32_t zero_partition_layout_device(const int64_t* numels_dev, int32_t n
                                             int32_t n_d, int32_t align, int64_t* scalars_dev,
                                             int64_t* tensor_offsets_dev, int64_t* shard_offsets_dev,
                                             zs_fragment* frags_dev, int64_t frag_cap, void* stream) {
+    zs::NvtxRange nvtx_range("zero_partition_layout_device");
     if (n_tensors < 0 || n_d < 1 || n_d > ZS_MAX_ND || !is_pow2(align) || frag_cap < 0)
         return ZS_ERR_ARG;
     if (scalars_dev == nullptr || shard_offsets_dev == nullptr) return ZS_ERR_ARG;

@@ -181,6 +181,7 @@ extern "C" {
 
 ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shards, int32_t n_d, const zs_sgd* hp,
                                          zs_ctrl* ctrl_dev, void* stream) {
+    zs::NvtxRange nvtx_range("zero_shard_step_sgd_async");
     if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS || n_d < 1 || n_d > ZS_MAX_ND ||
         !valid_sgd(hp) || ctrl_dev == nullptr)
         return ZS_ERR_ARG;

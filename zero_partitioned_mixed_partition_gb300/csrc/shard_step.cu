@@ -595,6 +595,7 @@ extern "C" {
 ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
                                int32_t* flag_dev, void* stream, int32_t* overflow_out) {
+    zs::NvtxRange nvtx_range("zero_shard_step");
     if (n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || !(loss_scale > 0.0) || loss_scale > 1e300 ||
         step < 1 || (cur != 0 && cur != 1) || flag_dev == nullptr || overflow_out == nullptr)
         return ZS_ERR_ARG;
@@ -667,6 +668,7 @@ static int32_t* noalloc_scratch(int32_t* status) {
 ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                        const zs_adam* hp, double loss_scale, int64_t step,
                                        int32_t cur, void* stream, int32_t* overflow_out) {
+    zs::NvtxRange nvtx_range("zero_shard_step_noalloc");
     if (n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || !(loss_scale > 0.0) || loss_scale > 1e300 ||
         step < 1 || (cur != 0 && cur != 1) || overflow_out == nullptr)
         return ZS_ERR_ARG;
@@ -745,6 +747,7 @@ ZS_API int32_t zero_step_commit_async(const zs_shard* shards, int32_t n_shards, 
 
 ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                      const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream) {
+    zs::NvtxRange nvtx_range("zero_shard_step_async");
     if (n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || ctrl_dev == nullptr) return ZS_ERR_ARG;
     if (!zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
     int width[ZS_MAX_SHARDS];
@@ -773,6 +776,7 @@ static void* mapped_host_pointer(const void* host) {
 
 ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
                                     zs_ctrl* ctrl_dev, void* stream, int32_t* overflow_out) {
+    zs::NvtxRange nvtx_range("zero_shard_step_host");
     if (shard == nullptr || n_d < 1 || n_d > ZS_MAX_ND || !valid_hp(hp) || ctrl_dev == nullptr ||
         overflow_out == nullptr)
         return ZS_ERR_ARG;

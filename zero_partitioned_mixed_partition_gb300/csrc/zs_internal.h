@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "zero_shard.h"
@@ -15,6 +16,15 @@ int32_t cuda_fail(cudaError_t err, const char* where);
 int32_t fail_with(int32_t status, const char* message);
 // Adds n to the count reported by zero_kernel_launches().
 void count_launches(int64_t n);
+
+// NVTX range around an entry point, so profiler timelines show each step
+// (header-only NVTX: a no-op unless a profiling tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 inline bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
