@@ -89,12 +89,24 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(kernel_source: str):
+KERNEL_SOURCES = [os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc", f)
+                  for f in ("shard_step.cu", "step_common.cuh")]
+
+
+def kernel_source_digest() -> str:
+    """sha256 prefix over the sources the fused step kernel is compiled from."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
     """DRAM bytes per stepped parameter from the committed ncu summary, valid
-    only while the kernel source is unchanged (else None)."""
+    only while the kernel sources are unchanged (else None)."""
     path = os.path.join(ROOT, "profiles", "shard_step_kernel_traffic.txt")
     try:
-        digest = hashlib.sha256(open(kernel_source, "rb").read()).hexdigest()[:16]
+        digest = kernel_source_digest()
         vals = {}
         for line in open(path):
             if ":" in line and not line.startswith("#"):
@@ -381,15 +393,6 @@ def main():
         norm_ms = [ev[0].elapsed_time(ev[2]) for ev in pairs]
         upd_ms = [ev[2].elapsed_time(ev[1]) for ev in pairs]
     ctrl = run.ctrl_host()
-    if args.log_steps:
-        path = args.log_steps if world == 1 else f"{args.log_steps}.rank{rank}"
-        bps = run.clipped_bytes_per_step() if clip else run.bytes_per_step()
-        with open(path, "w") as f:
-            for k, (ev, ms) in enumerate(zip(pairs, kern_ms)):
-                f.write(json.dumps({"rank": rank, "workload": w.name, "timed_step": k, "kernel_ms": round(ms, 5),
-                                    "kernel_gbs": round(bps / (ms / 1e3) / 1e9, 1),
-                                    "gparams_s": round(run.elements_per_step() / (ms / 1e3) / 1e9, 3)}) + "\n")
-            f.write(json.dumps({"rank": rank, "final_ctrl": ctrl}) + "\n")
     assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + args.warmup + args.steps, ctrl
 
     ms_max = zdist.max_over_ranks(ms_total, device=dev)
@@ -402,13 +405,25 @@ def main():
     if args.qwz:  # int8 codes + one fp32 scale per 256 elements, written by the step
         bytes_step += sum(run.n_valid[r] + 4 * ((run.n_valid[r] + 255) // 256) for r in run.shard_ids)
     hbm_gbs = bytes_step * world * args.steps / (ms_max / 1e3) / 1e9
+    if args.log_steps:
+        # one record per timed step; no step of the timed region overflowed
+        # (checked above), so t advances by one per step and L is constant
+        peak_gbs, _ = measured_peaks()
+        t_first = prewarm_steps + args.warmup + 1
+        path = args.log_steps if world == 1 else f"{args.log_steps}.rank{rank}"
+        with open(path, "w") as f:
+            for k, ms in enumerate(kern_ms):
+                gbs = bytes_step / (ms / 1e3) / 1e9
+                f.write(json.dumps({"workload": w.name, "n_d": w.n_d, "rank": rank, "t": t_first + k,
+                                    "overflow": 0, "loss_scale": ctrl["loss_scale"], "kernel_ms": round(ms, 5),
+                                    "gparams_s": round(elems / (ms / 1e3) / 1e9, 3), "kernel_gbs": round(gbs, 1),
+                                    "pct_of_peak": round(100 * gbs / peak_gbs, 2)}) + "\n")
     peak, peak_kind = measured_peaks()
 
     # roofline of the dominant kernel: algorithmic bytes per launch / mean launch time
     mean_kern_ms = statistics.mean(kern_ms)
     achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
-    traffic_per_param = recorded_traffic(os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc",
-                                                      "shard_step.cu"))
+    traffic_per_param = recorded_traffic()
     traffic = None
     if traffic_per_param and w.n_d in traffic_per_param and not clip and not args.qwz and args.optimizer == "adam":
         traffic = round(traffic_per_param[w.n_d] * elems)
