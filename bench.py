@@ -54,6 +54,9 @@ def parse_args():
                     help="adam (the pages' mixed-precision Adam) or sgd (SGD with momentum 0.9)")
     ap.add_argument("--qwz", action="store_true",
                     help="keep the int8 qwZ copy of the fp16 shard in each step (1 + 4/256 bytes per element)")
+    ap.add_argument("--math", default="fast", choices=["fast", "ieee"],
+                    help="rounding of the Adam update's last division: fast (ZS_MATH_FAST, corrected hardware "
+                         "reciprocal, within 1 ulp) or ieee (every operation IEEE, bit-exact)")
     ap.add_argument("--log-steps", default="",
                     help="write one JSON record per timed step (kernel ms, rank, workload) to this file")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -303,7 +306,8 @@ def main():
         w = dataclasses.replace(w, rank=zdist.replica_shard(w.rank, rank, w.n_d))
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        run = WorkloadRunner(w, dev, stream=stream)
+        run = WorkloadRunner(w, dev, stream=stream,
+                             math=binding.ZS_MATH_FAST if args.math == "fast" else binding.ZS_MATH_IEEE)
         numels_dev = torch.tensor(list(w.numels), dtype=torch.int64, device=dev)
         lay_scalars = torch.zeros(5, dtype=torch.int64, device=dev)
         lay_toff = torch.zeros(len(w.numels), dtype=torch.int64, device=dev)
@@ -456,6 +460,9 @@ def main():
         "config": {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
                    "bytes_per_param": round(bytes_step / max(elems, 1), 4), "bytes_per_step": bytes_step,
                    "storage": "fp16 grads and params, fp32 master/m/v (ping-pong)",
+                   "math": ("ZS_MATH_FAST: u by corrected hardware reciprocal (within 1 ulp), all else IEEE; "
+                            "m/v bit-exact" if args.math == "fast" else "ZS_MATH_IEEE: every fp32 operation IEEE, "
+                            "bit-exact"),
                    "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
                    if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -71,14 +71,43 @@ typedef struct zs_fragment {
     int64_t length;        /* elements, > 0 */
 } zs_fragment;
 
+/* Arithmetic of the Adam update's last division (zs_adam.math).
+ *
+ *   ZS_MATH_IEEE  every fp32 operation is one IEEE round-to-nearest step:
+ *                 mh = m / (1 - b1^t), vh = v / (1 - b2^t),
+ *                 u = mh / (sqrt(vh) + eps).  The results equal the plain
+ *                 definition bit for bit (and so the oracle of the tests).
+ *   ZS_MATH_FAST  permission to form u from the hardware reciprocal estimate
+ *                 of sqrt(vh) + eps with one fused-multiply-add residual
+ *                 correction instead of the IEEE divide.  u is then within
+ *                 1 ulp of the exact quotient and equal to the IEEE one
+ *                 except when the quotient lies extremely close to a rounding
+ *                 midpoint; the bias corrections, the square root, m and v are
+ *                 IEEE in both modes, so m and v are always bit-identical and
+ *                 master/params differ, rarely, by one rounding of lr * u.
+ *                 Taken by the 8-element layout and by the 16-element layout
+ *                 compiled for N_d = 16, 32 or 64 (the fused step without a
+ *                 qwZ copy, and the clipped step's update); the other kernels
+ *                 (scalar layout, the fused step's qwZ variant, the host-core
+ *                 step) run IEEE.
+ *
+ * "DeepSpeed ZeRO Stages", sec. 2.1, Fact 1 (the Adam step of each coordinate)
+ * names no rounding for these operations. */
+#define ZS_MATH_IEEE 0
+#define ZS_MATH_FAST 1
+
 /* Adam / AdamW hyper-parameters.  weight_decay = 0 gives plain Adam; a
- * positive value applies decoupled decay: theta -= lr * (u + wd * theta). */
+ * positive value applies decoupled decay: theta -= lr * (u + wd * theta).
+ * math is ZS_MATH_IEEE or ZS_MATH_FAST; reserved must be 0.  A zero-filled
+ * struct tail therefore selects the IEEE mode. */
 typedef struct zs_adam {
     double lr;
     double beta1;
     double beta2;
     double eps;
     double weight_decay;
+    int32_t math;
+    int32_t reserved;
 } zs_adam;
 
 /* SGD-with-momentum hyper-parameters (zero_shard_step_sgd_async). */

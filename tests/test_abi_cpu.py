@@ -142,6 +142,11 @@ def test_step_argument_checks_refuse_before_cuda(zs):
     assert call(flag=ctypes.c_void_p(0x20002)) == zs.ZS_ERR_ALIGN
     assert call(hp=zs.adam(1e-3, beta1=1.0)) == zs.ZS_ERR_ARG
     assert call(hp=zs.adam(float("nan"))) == zs.ZS_ERR_ARG
+    assert call(hp=zs.adam(1e-3, math=2)) == zs.ZS_ERR_ARG        # no such arithmetic mode
+    assert call(hp=zs.adam(1e-3, math=-1)) == zs.ZS_ERR_ARG
+    odd = zs.adam(1e-3, math=zs.ZS_MATH_FAST)
+    odd.reserved = 1
+    assert call(hp=odd) == zs.ZS_ERR_ARG
     bad, k1 = _fake_shard(n=-1)
     assert call(arr=(zs.Shard * 1)(bad)) == zs.ZS_ERR_ARG
     bad, k2 = _fake_shard(grads_ok=False)
@@ -171,3 +176,14 @@ def test_step_argument_checks_refuse_before_cuda(zs):
                                           ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), None, 0,
                                           None) == zs.ZS_ERR_ALIGN
     assert zs.zero_kernel_launches() == 0
+
+
+def test_adam_struct_layout(zs):
+    """zs_adam: five doubles, then the int32 arithmetic mode and a reserved
+    int32, 48 bytes; the binding's default is the IEEE mode."""
+    assert ctypes.sizeof(zs.Adam) == 48
+    assert zs.Adam.math.offset == 40 and zs.Adam.reserved.offset == 44
+    assert zs.adam(1e-3).math == zs.ZS_MATH_IEEE == 0
+    assert zs.adam(1e-3, math=zs.ZS_MATH_FAST).math == zs.ZS_MATH_FAST == 1
+    text = open(os.path.join(ROOT, "include", "zero_shard.h")).read()
+    assert re.search(r"#define ZS_MATH_IEEE 0\b", text) and re.search(r"#define ZS_MATH_FAST 1\b", text)

@@ -63,9 +63,11 @@ def _compare(run, refs, what):
 @pytest.mark.parametrize("n,n_d", [(2048 * 5 + 3, 4), (4099, 8), (20000, 16), (777, 64), (5000, 3)])
 @pytest.mark.parametrize("keep_g", [False, True])
 @pytest.mark.parametrize("max_norm_kind", ["active", "inactive", "off"])
-def test_clipped_step_matches_oracle(zs, oracle, cuda_device, n, n_d, keep_g, max_norm_kind):
+@pytest.mark.parametrize("math", ["ieee", "fast"])
+def test_clipped_step_matches_oracle(zs, oracle, cuda_device, n, n_d, keep_g, max_norm_kind, math):
+    """math = fast: ZS_MATH_FAST, the same tolerance; m and v stay bit-exact."""
     w = _workload(n, n_d)
-    run = WorkloadRunner(w, cuda_device)
+    run = WorkloadRunner(w, cuda_device, math=zs.ZS_MATH_FAST if math == "fast" else zs.ZS_MATH_IEEE)
     run.enable_clipping(keep_g)
     r = run.shard_ids[0]
     refs = [OracleShard(oracle, to_np(run.state[r][0][0]))]
@@ -88,14 +90,20 @@ def test_clipped_step_matches_oracle(zs, oracle, cuda_device, n, n_d, keep_g, ma
         else:
             assert c == 1.0
         assert run.ctrl_host()["step"] == applied
-        _compare(run, refs, f"step {step}")
+        _compare(run, refs, f"{math} step {step}")
+        _, m, v, _ = run.current(r)
+        assert np.array_equal(to_np(m[:n]).view(np.uint32), refs[0].m.view(np.uint32))
+        assert np.array_equal(to_np(v[:n]).view(np.uint32), refs[0].v.view(np.uint32))
 
 
-def test_clip_off_equals_unclipped_step(zs, cuda_device):
-    """max_norm <= 0: the clipped step is the plain step, bit for bit."""
-    n, n_d = 2048 * 3 + 1, 8
+@pytest.mark.parametrize("n_d,math", [(8, "ieee"), (4, "ieee"), (4, "fast"), (16, "fast")])
+def test_clip_off_equals_unclipped_step(zs, cuda_device, n_d, math):
+    """max_norm <= 0: the clipped step is the plain step, bit for bit, in
+    either arithmetic mode."""
+    n = 2048 * 3 + 1
     w = _workload(n, n_d, grads_fresh_per_step=False)
-    a, b = WorkloadRunner(w, cuda_device), WorkloadRunner(w, cuda_device)
+    mode = zs.ZS_MATH_FAST if math == "fast" else zs.ZS_MATH_IEEE
+    a, b = WorkloadRunner(w, cuda_device, math=mode), WorkloadRunner(w, cuda_device, math=mode)
     b.enable_clipping(True)
     for _ in range(3):
         a.step()

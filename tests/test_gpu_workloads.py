@@ -19,10 +19,14 @@ def _gather_bits(ts, idx_dev):
     return [synth.fp16_bits(t[idx_dev]) for t in ts]
 
 
+@pytest.mark.parametrize("math", ["ieee", "fast"])
 @pytest.mark.parametrize("name", ["tiny", "gpt2s", "ragged", "xl", "7b5"])
-def test_workload_full_size(zs, oracle, cuda_device, name):
+def test_workload_full_size(zs, oracle, cuda_device, name, math):
+    """math = fast runs ZS_MATH_FAST, as the benchmark does: the same bar
+    (master within tolerance, params within 1 fp16 ulp), and m, v bit-exact
+    (they involve no division)."""
     w = synth.WORKLOADS[name]
-    run = WorkloadRunner(w, cuda_device)
+    run = WorkloadRunner(w, cuda_device, math=zs.ZS_MATH_FAST if math == "fast" else zs.ZS_MATH_IEEE)
     samples, refs = {}, []
     for r in run.shard_ids:
         n = run.n_valid[r]
@@ -65,6 +69,8 @@ def test_workload_full_size(zs, oracle, cuda_device, name):
             master, m, v, params = run.current(r)
             i = samples[r]
             ref.compare(to_np(master[i]), to_np(m[i]), to_np(v[i]), f16_bits(params[i]),
-                        what=f"{name} shard {r} step {step}")
+                        what=f"{name} {math} shard {r} step {step}")
+            assert np.array_equal(to_np(m[i]).view(np.uint32), ref.m.view(np.uint32))
+            assert np.array_equal(to_np(v[i]).view(np.uint32), ref.v.view(np.uint32))
     if w.inf_at is not None:
         assert run.ctrl_host()["skipped"] == 1 and ls == w.loss_scale / 2

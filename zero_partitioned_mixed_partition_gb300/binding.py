@@ -24,6 +24,7 @@ ZS_MAX_ND = 1024
 ZS_MAX_SHARDS = 256
 ZS_NOALLOC_MAX_SHARDS = 64
 ZS_QWZ_BLOCK = 256
+ZS_MATH_IEEE, ZS_MATH_FAST = 0, 1
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -43,7 +44,8 @@ class Fragment(ctypes.Structure):
 
 
 class Adam(ctypes.Structure):
-    _fields_ = [("lr", _F64), ("beta1", _F64), ("beta2", _F64), ("eps", _F64), ("weight_decay", _F64)]
+    _fields_ = [("lr", _F64), ("beta1", _F64), ("beta2", _F64), ("eps", _F64), ("weight_decay", _F64),
+                ("math", _I32), ("reserved", _I32)]
 
 
 class Shard(ctypes.Structure):
@@ -254,8 +256,10 @@ def _shard_array(shards: Sequence[ShardView]):
 
 
 def adam(lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
-         weight_decay: float = 0.0) -> Adam:
-    return Adam(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay))
+         weight_decay: float = 0.0, math: int = None) -> Adam:
+    """Adam hyper-parameters; math is ZS_MATH_IEEE (default) or ZS_MATH_FAST."""
+    return Adam(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                ZS_MATH_IEEE if math is None else int(math), 0)
 
 
 def sgd(lr: float, momentum: float = 0.9, weight_decay: float = 0.0) -> Sgd:

@@ -131,8 +131,8 @@ __global__ void __launch_bounds__(kClipThreads) grad_norm_kernel(const __grid_co
     if (threadIdx.x == 0) atomicAdd(p.sqnorm, total);
 }
 
-// Pass 2: clipped Adam / AdamW update and fp16 cast.
-template <int CAP, int VEC, int ND>
+// Pass 2: clipped Adam / AdamW update and fp16 cast.  FAST: ZS_MATH_FAST.
+template <int CAP, int VEC, int ND, bool FAST>
 __global__ void __launch_bounds__(kClipThreads) clipped_step_kernel(const __grid_constant__ ClipArgs<CAP> p) {
     __shared__ Coef s_coef;
     __shared__ float s_clip;
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kClipThreads) clipped_step_kernel(const __grid
         if (p.g != nullptr) Mem<V>::load_f(p.g + e, g);
         else reduced_grad<CAP, V, ND>(p, c.inv, e, g);
 #pragma unroll
-        for (int j = 0; j < V; ++j) adam_apply(c, __fmul_rn(g[j], clip), th[j], m[j], v[j]);
+        for (int j = 0; j < V; ++j) adam_apply<FAST>(c, __fmul_rn(g[j], clip), th[j], m[j], v[j]);
         Mem<V>::store_f(th_out + e, th);
         Mem<V>::store_f(m_out + e, m);
         Mem<V>::store_f(v_out + e, v);
@@ -191,16 +191,26 @@ __global__ void __launch_bounds__(kClipThreads) clipped_step_kernel(const __grid
 
 enum class Pass { Norm, Update };
 
-template <int CAP, int VEC, int ND>
-int32_t launch_pass(Pass pass, const ClipArgs<CAP>& a, cudaStream_t stream) {
+template <int CAP, int VEC, int ND, bool FAST>
+int32_t launch_pass_as(Pass pass, const ClipArgs<CAP>& a, cudaStream_t stream) {
     const void* k = pass == Pass::Norm ? (const void*)grad_norm_kernel<CAP, VEC, ND>
-                                       : (const void*)clipped_step_kernel<CAP, VEC, ND>;
+                                       : (const void*)clipped_step_kernel<CAP, VEC, ND, FAST>;
     const int blocks = zs::persistent_blocks(k, kClipThreads, a.n / VEC > 0 ? a.n / VEC : 1);
     if (pass == Pass::Norm)
         grad_norm_kernel<CAP, VEC, ND><<<blocks, kClipThreads, 0, stream>>>(a);
     else
-        clipped_step_kernel<CAP, VEC, ND><<<blocks, kClipThreads, 0, stream>>>(a);
+        clipped_step_kernel<CAP, VEC, ND, FAST><<<blocks, kClipThreads, 0, stream>>>(a);
     return zs::check_launch(pass == Pass::Norm ? "grad_norm_kernel" : "clipped_step_kernel");
+}
+
+// ZS_MATH_FAST is taken by the same layouts as in the unclipped step: the
+// 8-element one and the 16-element one compiled for N_d = 16, 32, 64.
+template <int CAP, int VEC, int ND>
+int32_t launch_pass(Pass pass, const ClipArgs<CAP>& a, cudaStream_t stream) {
+    if constexpr (VEC == 8 || (VEC == 16 && ND > 0)) {
+        if (pass == Pass::Update && a.hp.math == ZS_MATH_FAST) return launch_pass_as<CAP, VEC, ND, true>(pass, a, stream);
+    }
+    return launch_pass_as<CAP, VEC, ND, false>(pass, a, stream);
 }
 
 template <int CAP, int ND>

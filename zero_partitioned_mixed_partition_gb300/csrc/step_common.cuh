@@ -51,19 +51,39 @@ __device__ __forceinline__ bool nonfinite(float x) {
     return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
 }
 
+// a / b for ZS_MATH_FAST: the hardware reciprocal estimate y ~ 1/b (PTX
+// rcp.approx, at most 1 ulp off), the quotient q0 = a * y, and one residual
+// correction q0 + (a - b q0) y with the residual formed exactly by a fused
+// multiply-add (the Newton-Raphson / Markstein correction step of FMA-based
+// division).  The result is within 1 ulp of a / b and equals the correctly
+// rounded quotient except when a / b lies extremely close to a rounding
+// midpoint.  b = sqrt(vh) + eps >= eps > 0 here.
+__device__ __forceinline__ float div_corrected(float a, float b) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(b));
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, b, a);
+    return __fmaf_rn(r, y, q0);
+}
+
 // One Adam / AdamW update of one coordinate from its reduced gradient g.
+// FAST (ZS_MATH_FAST) forms u with div_corrected instead of the IEEE divide;
+// everything else, m and v included, is the same in both modes.
+template <bool FAST>
 __device__ __forceinline__ void adam_apply(const Coef& c, float g, float& th, float& m, float& v) {
     m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.c1, g));
     v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.c2, __fmul_rn(g, g)));
     const float mh = __fdiv_rn(m, c.bc1);
     const float vh = __fdiv_rn(v, c.bc2);
-    const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), c.eps));
+    const float den = __fadd_rn(__fsqrt_rn(vh), c.eps);
+    const float u = FAST ? div_corrected(mh, den) : __fdiv_rn(mh, den);
     th = __fsub_rn(th, __fmul_rn(c.lr, __fadd_rn(u, __fmul_rn(c.wd, th))));
 }
 
 // The same from the summed contributions gs: g = gs * (float)(1 / (N_d L)).
+template <bool FAST>
 __device__ __forceinline__ void adam_update(const Coef& c, float gs, float& th, float& m, float& v) {
-    adam_apply(c, __fmul_rn(gs, c.inv), th, m, v);
+    adam_apply<FAST>(c, __fmul_rn(gs, c.inv), th, m, v);
 }
 
 // --------------------------------------------------------- vector memory ---

@@ -25,7 +25,7 @@ class WorkloadRunner:
 
     def __init__(self, w: synth.Workload, device, shards: Optional[Sequence[int]] = None,
                  with_full_params: bool = True,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None, math: int = binding.ZS_MATH_IEEE):
         self.w = w
         self.device = torch.device(device)
         self.stream = stream
@@ -38,7 +38,7 @@ class WorkloadRunner:
         fr = lay["fragments"]
         valid = np.bincount(fr["shard"], weights=fr["length"], minlength=w.n_d).astype(np.int64)
         self.n_valid = {r: int(valid[r]) for r in self.shard_ids}
-        self.hp = binding.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+        self.hp = binding.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, math=math)
 
         nshards_full = w.n_d if with_full_params else len(self.shard_ids)
         self.params_full = torch.zeros(nshards_full * self.S, dtype=torch.float16, device=self.device)
