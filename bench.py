@@ -490,6 +490,10 @@ def main():
         line["cpu_baseline"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th, "kind": "oracle",
                                 "sample": f"{min(4_000_000, elems):,} params of the shard x N_d={w.n_d}, "
                                           f"{steps} steps in {el:.1f} s over {th} threads"}
+        g1, steps1, el1, _ = oracle_throughput(w, min(1_000_000, elems), 3.0, 1)
+        line["cpu_baseline"]["single_thread"] = {
+            "value": round(g1, 4), "unit": "Gparams/s", "cores": 1,
+            "sample": f"{min(1_000_000, elems):,} params x N_d={w.n_d}, {steps1} steps in {el1:.1f} s on one thread"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ns = min(32_000_000, elems)
         g, steps, el, th = native_cpu_throughput(w, ns, 3.0, os.cpu_count() or 1)

@@ -87,9 +87,9 @@ typedef struct zs_fragment {
  *                 master/params differ, rarely, by one rounding of lr * u.
  *                 Taken by the 8-element layout and by the 16-element layout
  *                 compiled for N_d = 16, 32 or 64 (the fused step without a
- *                 qwZ copy, and the clipped step's update); the other kernels
- *                 (scalar layout, the fused step's qwZ variant, the host-core
- *                 step) run IEEE.
+ *                 qwZ copy, and the clipped step's update); the scalar layout,
+ *                 the run-time-N_d 16-element layout, the fused step with a
+ *                 qwZ copy and the host-core step run IEEE.
  *
  * "DeepSpeed ZeRO Stages", sec. 2.1, Fact 1 (the Adam step of each coordinate)
  * names no rounding for these operations. */

@@ -38,9 +38,13 @@ def _check_codes(oracle, run, r, ref_params_bits, what):
 
 @pytest.mark.parametrize("n", [256 * 40, 256 * 40 + 77, 200, 4096 * 3 + 8])
 @pytest.mark.parametrize("n_d", [4, 8, 64])
-def test_fused_qwz_matches_oracle(zs, oracle, cuda_device, n, n_d):
+@pytest.mark.parametrize("math", ["ieee", "fast"])
+def test_fused_qwz_matches_oracle(zs, oracle, cuda_device, n, n_d, math):
+    """math = fast (ZS_MATH_FAST): params within the stated tolerance of the
+    oracle's, and the codes equal to the oracle's quantization of the kernel's
+    own fp16 shard (the same fp32 decision on the same inputs)."""
     w = _workload(n, n_d)
-    run = WorkloadRunner(w, cuda_device)
+    run = WorkloadRunner(w, cuda_device, math=zs.ZS_MATH_FAST if math == "fast" else zs.ZS_MATH_IEEE)
     run.enable_qwz()
     r = run.shard_ids[0]
     ref = OracleShard(oracle, to_np(run.state[r][0][0]))
@@ -58,7 +62,10 @@ def test_fused_qwz_matches_oracle(zs, oracle, cuda_device, n, n_d):
         assert ovf == int(step == 3) == run.ctrl_host()["last_overflow"]
         master, m, v, params = run.current(r)
         ref.compare(to_np(master), to_np(m), to_np(v), f16_bits(params), what=f"step {step}")
-        _check_codes(oracle, run, r, ref.params, f"n={n} n_d={n_d} step {step}")
+        own = f16_bits(params[:n])
+        if math == "ieee":
+            assert np.array_equal(own, ref.params[:n])
+        _check_codes(oracle, run, r, own, f"{math} n={n} n_d={n_d} step {step}")
 
 
 @pytest.mark.parametrize("offset", [0, 1])

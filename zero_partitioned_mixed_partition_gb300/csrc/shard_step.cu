@@ -535,15 +535,16 @@ int32_t launch_step_vec(const StepArgs<CAP>& a, cudaStream_t stream) {
     return zs::check_launch("shard_step_kernel");
 }
 
-// Without a qwZ copy, ZS_MATH_FAST runs the FAST instantiation where it
-// measured faster: the 8-element layout (N_d = 4: +5.6 %, 6.76 TB/s) and the
-// 16-element layout compiled for N_d = 16, 32, 64 (+1.3 % at 16).
-template <int CAP, int VEC, int ND>
-int32_t launch_plain(const StepArgs<CAP>& a, bool fast, cudaStream_t stream) {
-    if constexpr (VEC == 8 || (VEC == 16 && ND > 0)) {
-        if (fast) return launch_step_vec<CAP, VEC, ND, false, true>(a, stream);
+// ZS_MATH_FAST runs the FAST instantiation where it measured faster: the
+// 8-element layout (N_d = 4: +5.6 %, 6.76 TB/s) and the 16-element layout
+// compiled for N_d = 16, 32, 64 (+1.3 % at 16), without a qwZ copy (with one,
+// the 8-element kernel measured no gain: 172.4 vs 173.4 Gparams/s at N_d = 4).
+template <int CAP, int VEC, int ND, bool QZ>
+int32_t launch_math(const StepArgs<CAP>& a, bool fast, cudaStream_t stream) {
+    if constexpr (!QZ && (VEC == 8 || (VEC == 16 && ND > 0))) {
+        if (fast) return launch_step_vec<CAP, VEC, ND, QZ, true>(a, stream);
     }
-    return launch_step_vec<CAP, VEC, ND, false>(a, stream);
+    return launch_step_vec<CAP, VEC, ND, QZ>(a, stream);
 }
 
 // CAP sizes the contribution table; ND > 0 compiles the kernel for exactly ND
@@ -573,10 +574,10 @@ int32_t launch_step_cap(const zs_shard& s, int32_t n_d, int width, const Coef* c
     // the wide layout only pays once N_d > 4 (measured); scalar if misaligned
     if constexpr (ND == 0 || ND > 4) {
         if (width == 2 && n_d > 4)
-            return qz ? launch_step_vec<CAP, 16, ND, true>(a, stream) : launch_plain<CAP, 16, ND>(a, fast, stream);
+            return qz ? launch_math<CAP, 16, ND, true>(a, fast, stream) : launch_math<CAP, 16, ND, false>(a, fast, stream);
     }
     if (width >= 1)
-        return qz ? launch_step_vec<CAP, 8, ND, true>(a, stream) : launch_plain<CAP, 8, ND>(a, fast, stream);
+        return qz ? launch_math<CAP, 8, ND, true>(a, fast, stream) : launch_math<CAP, 8, ND, false>(a, fast, stream);
     // scalar kernel: the qwZ copy of every block follows in its own pass
     int32_t rc = launch_step_vec<CAP, 1, ND, false>(a, stream);
     if (rc == ZS_OK && qz)
