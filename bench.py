@@ -42,6 +42,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="xl", help="tiny | gpt2s | ragged | xl | 7b5")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--rank", type=int, default=None,
+                    help="simulated rank whose shard is stepped (default: the workload's; the ragged "
+                         "workload steps all shards unless a rank is given)")
     ap.add_argument("--shard-params", type=int, default=0,
                     help="shrink the workload to this many params per shard (profiling runs)")
     ap.add_argument("--prewarm-s", type=float, default=3.0,
@@ -74,6 +77,10 @@ def workload(args):
     w = synth.WORKLOADS[args.workload]
     if args.shard_params:
         w = dataclasses.replace(w, name=f"{w.name}-small", numels=(args.shard_params * w.n_d,), align=128)
+    if args.rank is not None:
+        if not 0 <= args.rank < w.n_d:
+            raise SystemExit(f"--rank must be in [0, {w.n_d})")
+        w = dataclasses.replace(w, rank=args.rank)
     return w
 
 

@@ -423,6 +423,18 @@ ZS_API const char* zero_last_error(void);
 /* Number of kernels this library has enqueued in this process. */
 ZS_API int64_t zero_kernel_launches(void);
 
+/* Index checks of the debug build.  The same sources compiled with
+ * ZS_CHECKED=1 give libzeroshard_checked.so, whose kernels test every element
+ * range they are about to touch against the extent the call was given (the
+ * shard's n, or its qwZ block count); a failed test records the first failure
+ * -- (site << 48) | first element, site 1-9 naming the kernel and access --
+ * and skips the access instead of trapping.  This call synchronises the
+ * device, writes that record (0: none) to *first_fault, clears it, and
+ * returns 1 in the checked build; the ordinary build has no checks and
+ * returns 0 with *first_fault = 0.  ZS_ERR_ARG if first_fault is NULL,
+ * ZS_ERR_CUDA if the record cannot be read. */
+ZS_API int32_t zero_debug_checks(uint64_t* first_fault);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,9 +24,21 @@ def zs():
     """The product binding with its CUDA library built (nvcc cross-compiles
     without a GPU; loading the library needs no device)."""
     from zero_partitioned_mixed_partition_gb300 import binding, build
-    build.build()
+    build.build(checked=os.environ.get("ZS_CHECKED") == "1")
     binding.lib()
     return binding
+
+
+@pytest.fixture(autouse=True)
+def _index_checks(request):
+    """Under the debug build (ZS_CHECKED=1), every GPU test must leave the
+    kernels' index checks without a recorded failure."""
+    yield
+    if os.environ.get("ZS_CHECKED") == "1" and request.node.get_closest_marker("gpu"):
+        from zero_partitioned_mixed_partition_gb300 import binding
+        built, fault = binding.zero_debug_checks()
+        assert built, "ZS_CHECKED=1 but the loaded library has no index checks"
+        assert fault == 0, f"index check failed: site {fault >> 48}, element {fault & ((1 << 48) - 1)}"
 
 
 @pytest.fixture(scope="session")

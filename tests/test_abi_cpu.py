@@ -187,3 +187,12 @@ def test_adam_struct_layout(zs):
     assert zs.adam(1e-3, math=zs.ZS_MATH_FAST).math == zs.ZS_MATH_FAST == 1
     text = open(os.path.join(ROOT, "include", "zero_shard.h")).read()
     assert re.search(r"#define ZS_MATH_IEEE 0\b", text) and re.search(r"#define ZS_MATH_FAST 1\b", text)
+
+
+def test_debug_checks_absent_from_ordinary_build(zs):
+    """The ordinary library has no index checks: zero_debug_checks reports so
+    without touching the device; a NULL output pointer is refused."""
+    if os.environ.get("ZS_CHECKED") == "1":
+        pytest.skip("the debug build is loaded")
+    assert zs.zero_debug_checks() == (False, 0)
+    assert zs.lib().zero_debug_checks(None) == zs.ZS_ERR_ARG

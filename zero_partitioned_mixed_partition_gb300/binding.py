@@ -17,7 +17,9 @@ import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libzeroshard.so")
+# ZS_CHECKED=1 in the environment selects the debug build (kernel index checks)
+LIB_PATH = os.path.join(_PKG, "libzeroshard_checked.so" if os.environ.get("ZS_CHECKED") == "1"
+                        else "libzeroshard.so")
 
 ZS_OK, ZS_ERR_ARG, ZS_ERR_ALIGN, ZS_ERR_CUDA, ZS_ERR_TIMEOUT = 0, -1, -2, -3, -4
 ZS_MAX_ND = 1024
@@ -93,6 +95,7 @@ _SIGNATURES = {
     "zero_status_string": (ctypes.c_char_p, [_I32]),
     "zero_last_error": (ctypes.c_char_p, []),
     "zero_kernel_launches": (_I64, []),
+    "zero_debug_checks": (_I32, [_P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -126,6 +129,16 @@ def zero_last_error() -> str:
 
 def zero_kernel_launches() -> int:
     return int(lib().zero_kernel_launches())
+
+
+def zero_debug_checks():
+    """(built with index checks, first recorded failure or 0); clears the
+    record and synchronises the device."""
+    out = ctypes.c_uint64(0)
+    rc = int(lib().zero_debug_checks(ctypes.byref(out)))
+    if rc < 0:
+        _check(rc, "zero_debug_checks")
+    return rc == 1, int(out.value)
 
 
 def _check(rc: int, what: str):

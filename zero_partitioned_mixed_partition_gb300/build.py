@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libzeroshard.so")
+# the debug build: the same sources with the kernels' index checks compiled in
+CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
+CHECKED_LIB_PATH = os.path.join(PKG, "libzeroshard_checked.so")
 
 SOURCES = ["shard_step.cu", "clip.cu", "sgd.cu", "layout.cu", "cpu_step.cpp", "diag.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -36,23 +39,29 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(lib_path: str) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "zero_shard.h"), __file__]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every source and link ``libzeroshard.so``; returns its path."""
-    if not force and not _stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Compile every source and link ``libzeroshard.so`` (``checked``: the
+    debug build ``libzeroshard_checked.so``, with the kernels' index checks);
+    returns its path."""
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    build_dir = CHECKED_BUILD_DIR if checked else BUILD_DIR
+    if checked:
+        extra_flags = (*extra_flags, "-DZS_CHECKED=1")
+    if not force and not _stale(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     exe = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [exe, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -65,14 +74,22 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [exe, *ARCH, "-shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build_all(force: bool = False) -> tuple:
+    """Both libraries, compiled side by side."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        a = ex.submit(build, force)
+        b = ex.submit(build, force, False, (), True)
+        return a.result(), b.result()
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

@@ -102,6 +102,7 @@ __device__ __forceinline__ double sum_squares(const float* g) {
 template <int CAP, int VEC, int ND>
 __device__ __forceinline__ uint32_t norm_elements(const ClipArgs<CAP>& p, float inv, int64_t e, double& sq) {
     float g[VEC];
+    if (!ZS_RANGE_OK(kSiteNorm, e, VEC, p.n)) return 0u;
     const uint32_t bad = reduced_grad<CAP, VEC, ND>(p, inv, e, g);
     sq = __dadd_rn(sq, sum_squares<VEC>(g));
     if (p.g != nullptr) Mem<VEC>::store_f(p.g + e, g);
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kClipThreads) clipped_step_kernel(const __grid
     auto step = [&](auto vec_tag, int64_t e) {
         constexpr int V = decltype(vec_tag)::value;
         float th[V], m[V], v[V], g[V];
+        if (!ZS_RANGE_OK(kSiteClipped, e, V, p.n)) return;
         Mem<V>::load_f(th_in + e, th);
         Mem<V>::load_f(m_in + e, m);
         Mem<V>::load_f(v_in + e, v);
@@ -275,6 +277,10 @@ int32_t check_with_g(const zs_shard& s, int32_t n_d, const float* g, int* width)
 }
 
 }  // namespace
+
+namespace zs {
+uint64_t take_fault_clip() { return take_fault(); }
+}  // namespace zs
 
 extern "C" {
 

@@ -63,6 +63,21 @@ ZS_API const char* zero_last_error(void) { return zs::g_last_error.c_str(); }
 
 ZS_API int64_t zero_kernel_launches(void) { return zs::g_launches.load(std::memory_order_relaxed); }
 
+ZS_API int32_t zero_debug_checks(uint64_t* first_fault) {
+    if (first_fault == nullptr) return ZS_ERR_ARG;
+    *first_fault = 0;
+#if ZS_CHECKED
+    const uint64_t faults[] = {zs::take_fault_shard_step(), zs::take_fault_clip(), zs::take_fault_sgd()};
+    for (uint64_t f : faults) {
+        if (f == ~0ull) return zs::fail_with(ZS_ERR_CUDA, "zero_debug_checks: the fault record could not be read");
+        if (f != 0 && *first_fault == 0) *first_fault = f;
+    }
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 // Model-state bytes per device ("DeepSpeed ZeRO Stages", sec. 1.2 and 3):
 // three categories -- fp16 parameters (2 Psi), fp16 gradients (2 Psi) and
 // optimizer states (K Psi) -- and the stages partition them cumulatively,

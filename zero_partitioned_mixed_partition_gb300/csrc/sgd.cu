@@ -46,6 +46,7 @@ __device__ __forceinline__ uint32_t sgd_elements(const SgdArgs<CAP>& p, float in
                                                  int64_t e, const float* th_in, const float* b_in,
                                                  float* th_out, float* b_out) {
     float th[VEC], b[VEC], acc[VEC];
+    if (!ZS_RANGE_OK(kSiteSgd, e, VEC, p.n)) return 0u;
     Mem<VEC>::load_f(th_in + e, th);
     Mem<VEC>::load_f(b_in + e, b);
 #pragma unroll
@@ -176,6 +177,10 @@ bool valid_sgd(const zs_sgd* hp) {
 }
 
 }  // namespace
+
+namespace zs {
+uint64_t take_fault_sgd() { return take_fault(); }
+}  // namespace zs
 
 extern "C" {
 

@@ -69,6 +69,7 @@ __device__ __forceinline__ uint32_t step_elements(const StepArgs<CAP>& p, const 
                                                   const float* v_in, float* th_out, float* m_out,
                                                   float* v_out, float* th) {
     float m[VEC], v[VEC], acc[VEC];
+    if (!ZS_RANGE_OK(kSiteStep, e, VEC, p.n)) return 0u;
     Mem<VEC>::load_f(th_in + e, th);
     Mem<VEC>::load_f(m_in + e, m);
     Mem<VEC>::load_f(v_in + e, v);
@@ -140,8 +141,9 @@ __global__ void __launch_bounds__(kThreads) shard_step_kernel(const __grid_const
             const float scale = qwz_group_codes<VEC, G>(x, active ? VEC : 0, q);
             const int64_t block = (i0 + (lane & ~(G - 1))) * VEC / kQwzBlock;
             if ((block + 1) * kQwzBlock <= p.n) {  // full block: every lane of the group is active
-                store_codes<VEC>(p.qcodes + i * VEC, q);
-                if ((lane & (G - 1)) == 0) p.qscales[block] = scale;
+                if (ZS_RANGE_OK(kSiteQwzFused, i * VEC, VEC, p.n)) store_codes<VEC>(p.qcodes + i * VEC, q);
+                if ((lane & (G - 1)) == 0 && ZS_RANGE_OK(kSiteScale, block, 1, (p.n + kQwzBlock - 1) / kQwzBlock))
+                    p.qscales[block] = scale;
             }
         }
     }
@@ -183,6 +185,7 @@ __device__ __forceinline__ void cast_range(const float* master, uint16_t* params
         const int64_t nvec = n / 8;
         for (int64_t i = tid; i < nvec; i += stride) {
             float x[8];
+            if (!ZS_RANGE_OK(kSiteCast, 8 * i, 8, n)) continue;
             Mem<8>::load_f(master + 8 * i, x);
             Mem<8>::store_h(params + 8 * i, x);
         }
@@ -190,6 +193,7 @@ __device__ __forceinline__ void cast_range(const float* master, uint16_t* params
     }
     for (int64_t j = done + tid; j < n; j += stride) {
         float x[1];
+        if (!ZS_RANGE_OK(kSiteCast, j, 1, n)) continue;
         Mem<1>::load_f(master + j, x);
         Mem<1>::store_h(params + j, x);
     }
@@ -208,9 +212,15 @@ __device__ void qwz_blocks(const float* master, uint16_t* params, int64_t n, int
     for (int64_t b = b0 + gw; b < b1; b += nw) {
         const int64_t e0 = b * kQwzBlock + 8 * lane;
         const int64_t left = n - e0;
-        const int valid = left <= 0 ? 0 : (left >= 8 ? 8 : (int)left);
+        int valid = left <= 0 ? 0 : (left >= 8 ? 8 : (int)left);
+        // b is the same in every lane of the warp, so this skip keeps the warp
+        // together for the shuffles below; a failed element check only empties
+        // the lane (it still takes part in the block's max)
+        if (!ZS_RANGE_OK(kSiteScale, b, 1, (n + kQwzBlock - 1) / kQwzBlock)) continue;
+        const bool in_range = valid == 0 || ZS_RANGE_OK(kSiteQwz, e0, valid, n);
+        if (!in_range) valid = 0;
         float x[8];
-        if (vec && (b + 1) * kQwzBlock <= n) {
+        if (vec && (b + 1) * kQwzBlock <= n && in_range) {
             if (master != nullptr) {
                 Mem<8>::load_f(master + e0, x);
                 Mem<8>::store_h(params + e0, x);
@@ -318,6 +328,7 @@ __global__ void __launch_bounds__(kCastThreads) dequant_kernel(const int8_t* cod
     if (vec) {
         const int64_t nvec = n / 8;
         for (int64_t i = tid; i < nvec; i += stride) {
+            if (!ZS_RANGE_OK(kSiteDequant, 8 * i, 8, n)) continue;
             const uint2 w = *reinterpret_cast<const uint2*>(codes + 8 * i);
             const float s = scales[(8 * i) / kQwzBlock];
             float x[8];
@@ -332,6 +343,7 @@ __global__ void __launch_bounds__(kCastThreads) dequant_kernel(const int8_t* cod
         done = nvec * 8;
     }
     for (int64_t j = done + tid; j < n; j += stride) {
+        if (!ZS_RANGE_OK(kSiteDequant, j, 1, n)) continue;
         float x[1] = {__fmul_rn((float)codes[j], scales[j / kQwzBlock])};
         Mem<1>::store_h(params + j, x);
     }
@@ -604,6 +616,10 @@ int32_t launch_step(const zs_shard& s, int32_t n_d, int width, const Coef* coef,
 }
 
 }  // namespace
+
+namespace zs {
+uint64_t take_fault_shard_step() { return take_fault(); }
+}  // namespace zs
 
 extern "C" {
 

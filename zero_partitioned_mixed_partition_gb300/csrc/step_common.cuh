@@ -4,6 +4,41 @@
 // <cuda_fp16.h>, <stdint.h> and zero_shard.h.
 #pragma once
 
+// ------------------------------------------------------------ index checks ---
+
+// Debug build (compiled with ZS_CHECKED=1, libzeroshard_checked.so): before an
+// access of `count` elements starting at element `first`, ZS_RANGE_OK tests
+// 0 <= first and first + count <= limit, the extent the call was given (the
+// shard's n, or its qwZ block count).  A failed test records
+// (site << 48) | first in this translation unit's fault word -- the first
+// failure wins -- and the caller skips the access; nothing traps or asserts.
+// In the ordinary build ZS_RANGE_OK is the constant true.
+constexpr uint32_t kSiteStep = 1, kSiteQwzFused = 2, kSiteCast = 3, kSiteQwz = 4, kSiteDequant = 5,
+                   kSiteNorm = 6, kSiteClipped = 7, kSiteSgd = 8, kSiteScale = 9;
+
+#if ZS_CHECKED
+__device__ unsigned long long g_fault;
+
+__device__ __forceinline__ bool zs_range_ok(uint32_t site, int64_t first, int64_t count, int64_t limit) {
+    if (first >= 0 && count >= 0 && first + count <= limit) return true;
+    atomicCAS(&g_fault, 0ull, ((unsigned long long)site << 48) | ((unsigned long long)first & 0xffffffffffffull));
+    return false;
+}
+#define ZS_RANGE_OK(site, first, count, limit) zs_range_ok((site), (first), (count), (limit))
+
+// The recorded failure (0: none), cleared; synchronises the device.
+uint64_t take_fault() {
+    unsigned long long v = 0, zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ~0ull;
+    if (cudaMemcpyFromSymbol(&v, g_fault, sizeof(v)) != cudaSuccess) return ~0ull;
+    if (cudaMemcpyToSymbol(g_fault, &zero, sizeof(zero)) != cudaSuccess) return ~0ull;
+    return v;
+}
+#else
+#define ZS_RANGE_OK(site, first, count, limit) true
+uint64_t take_fault() { return 0; }
+#endif
+
 // ------------------------------------------------------------ coefficients ---
 
 // Scalar coefficients of one step, each formed in double and rounded once to

@@ -53,6 +53,12 @@ int32_t check_shard_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, 
 // first when master != nullptr).
 int32_t launch_qwz(const float* master, uint16_t* params, int64_t n, int8_t* codes, float* scales, int64_t b0,
                    int64_t b1, cudaStream_t stream);
+// The first index-check failure recorded by the kernels of each translation
+// unit (checked build only; 0 = none, ~0 = the record could not be read),
+// cleared on read.
+uint64_t take_fault_shard_step();
+uint64_t take_fault_clip();
+uint64_t take_fault_sgd();
 // Enqueues the device-side commit / skip of a step over `shards`.
 int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
                       cudaStream_t stream);
