@@ -89,8 +89,19 @@ __device__ __forceinline__ uint32_t step_elements(const StepArgs<CAP>& p, const 
     return bad;
 }
 
+// Minimum resident blocks per SM promised to the compiler (0: none).  The
+// 16-element kernels run two blocks per SM (about 100-128 registers each).  With
+// the qwZ epilogue and at most 16 compiled contributions the compiler left ~100
+// registers unused by default; promising two blocks lets it use the 128 they
+// have: +6.8 % on the ragged workload's qwZ step, +24 % at N_d = 8 (measured).
+// With 32 or 64 contributions it already uses 128, and the promise measured
+// 2.8 % slower there, so it is not made.
+template <int VEC, int ND, bool QZ>
+constexpr int step_min_blocks() { return (VEC == 16 && QZ && ND <= 16) ? 2 : 0; }
+
 template <int CAP, int VEC, int ND, bool QZ, bool FAST>
-__global__ void __launch_bounds__(kThreads) shard_step_kernel(const __grid_constant__ StepArgs<CAP> p) {
+__global__ void __launch_bounds__(kThreads, step_min_blocks<VEC, ND, QZ>())
+shard_step_kernel(const __grid_constant__ StepArgs<CAP> p) {
     __shared__ Coef s_coef;
     __shared__ int s_cur;
     if (threadIdx.x == 0) {

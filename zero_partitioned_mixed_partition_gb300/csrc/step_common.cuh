@@ -260,6 +260,21 @@ __device__ __forceinline__ void sum_contributions(const uint16_t* const (&grads)
 // Parameters per quantization block of the int8 copy of the fp16 shard.
 constexpr int kQwzBlock = ZS_QWZ_BLOCK;
 
+// x / s rounded once, for the codes of the 16-element layout: with the
+// correctly rounded reciprocal y = 1/s, q0 = x y and one exact-residual
+// correction q0 + (x - s q0) y (Markstein's theorem: the result is the
+// correctly rounded quotient when y is, and nothing under- or overflows).
+// Checked exhaustively on the domain it serves -- every fp16 x with |x| <= a
+// against every positive finite fp16 block maximum a, s = fp32(a / 127):
+// 1,007,713,278 pairs, all equal to the IEEE quotient.  Cheaper than a
+// divide per element in the 16-element kernels (+2.4 % on the ragged
+// workload's qwZ step, +6.5 % at N_d = 8); the 8-element kernel measured
+// faster with the IEEE divide and keeps it.
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+    const float q0 = __fmul_rn(x, y);
+    return __fmaf_rn(__fmaf_rn(-q0, s, x), y, q0);
+}
+
 // One quantization block held by an aligned group of G lanes, V consecutive
 // values per lane (G * V == kQwzBlock): the block's scale max|x| / 127 and this
 // lane's V codes rint(x / scale), ties to even, all in fp32.  Lanes past the
@@ -274,11 +289,21 @@ __device__ __forceinline__ float qwz_group_codes(const float* x, int valid, int8
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float scale = __fdiv_rn(amax, 127.0f);
+    if constexpr (V == 16) {
+        const float y = scale > 0.0f ? __frcp_rn(scale) : 0.0f;
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-        float r = scale > 0.0f ? rintf(__fdiv_rn(x[j], scale)) : 0.0f;
-        r = fminf(fmaxf(r, -127.0f), 127.0f);
-        q[j] = (int8_t)(int)r;
+        for (int j = 0; j < V; ++j) {
+            float r = scale > 0.0f ? rintf(div_by_scale(x[j], scale, y)) : 0.0f;
+            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            q[j] = (int8_t)(int)r;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            float r = scale > 0.0f ? rintf(__fdiv_rn(x[j], scale)) : 0.0f;
+            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            q[j] = (int8_t)(int)r;
+        }
     }
     return scale;
 }
