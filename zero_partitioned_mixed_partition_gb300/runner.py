@@ -14,6 +14,30 @@ import torch
 from . import binding, synth
 
 
+class _Arena:
+    """One device allocation carved into buffers of the given (numel, dtype),
+    handed out in order by take(); every buffer starts on a 2 MiB boundary."""
+
+    ALIGN = 2 << 20
+
+    def __init__(self, device, specs):
+        self.specs = list(specs)
+        sizes = [(n * torch.tensor([], dtype=dt).element_size() + self.ALIGN - 1) // self.ALIGN * self.ALIGN
+                 for n, dt in self.specs]
+        self.offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+        self.storage = torch.empty(int(self.offsets[-1]), dtype=torch.uint8, device=device)
+        self.next = 0
+
+    def take(self, dtype) -> torch.Tensor:
+        n, dt = self.specs[self.next]
+        if dt != dtype:
+            raise RuntimeError(f"arena buffer {self.next} is {dt}, {dtype} was asked for")
+        off = int(self.offsets[self.next])
+        self.next += 1
+        nbytes = n * torch.tensor([], dtype=dt).element_size()
+        return self.storage[off:off + nbytes].view(dt)
+
+
 class WorkloadRunner:
     """Simulates one or more ranks of a workload on one GPU.
 
@@ -45,14 +69,28 @@ class WorkloadRunner:
         self.grads = {}
         self.state = {}
         self.views: List[binding.ShardView] = []
+        # One arena for every stepped shard's N_d contributions and both state
+        # sets, each buffer starting on a 2 MiB boundary.  Measured on the
+        # 375M-parameter N_d = 4 shard: 6.90 TB/s for the fused kernel in six
+        # of six fresh processes, against 6.70-6.73 TB/s with one allocation
+        # per buffer (and 6.44 in some processes): the eleven streams the
+        # kernel walks then sit in one contiguous mapping.
+        per_shard = [(self.S, torch.float16)] * w.n_d + [(self.S, torch.float32)] * 6
+        arena = _Arena(self.device, per_shard * len(self.shard_ids))
+        self._arena = arena
         for i, r in enumerate(self.shard_ids):
             n = self.n_valid[r]
-            g = [synth.grad_contribution(w, n, k, 1, shard=r, device=self.device, n_alloc=self.S)
-                 for k in range(w.n_d)]
-            master0 = synth.master_init(w, n, shard=r, device=self.device, n_alloc=self.S)
-            master = (master0, torch.zeros_like(master0))
-            m = (torch.zeros_like(master0), torch.zeros_like(master0))
-            v = (torch.zeros_like(master0), torch.zeros_like(master0))
+            g = []
+            for k in range(w.n_d):
+                buf = arena.take(torch.float16)
+                buf.copy_(synth.grad_contribution(w, n, k, 1, shard=r, device=self.device, n_alloc=self.S))
+                g.append(buf)
+            master0 = arena.take(torch.float32)
+            master0.copy_(synth.master_init(w, n, shard=r, device=self.device, n_alloc=self.S))
+            f32 = lambda: arena.take(torch.float32).zero_()
+            master = (master0, f32())
+            m = (f32(), f32())
+            v = (f32(), f32())
             slot = r if with_full_params else i
             params = self.params_full[slot * self.S:(slot + 1) * self.S]
             self.grads[r] = g
