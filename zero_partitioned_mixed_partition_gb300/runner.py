@@ -70,11 +70,12 @@ class WorkloadRunner:
         self.state = {}
         self.views: List[binding.ShardView] = []
         # One arena for every stepped shard's N_d contributions and both state
-        # sets, each buffer starting on a 2 MiB boundary.  Measured on the
-        # 375M-parameter N_d = 4 shard: 6.90 TB/s for the fused kernel in six
-        # of six fresh processes, against 6.70-6.73 TB/s with one allocation
-        # per buffer (and 6.44 in some processes): the eleven streams the
-        # kernel walks then sit in one contiguous mapping.
+        # sets, each buffer starting on a 2 MiB boundary: one allocation and a
+        # layout that does not depend on the allocator's history.  On the
+        # 375M-parameter N_d = 4 shard the fused kernel ran at 6.76-6.80 TB/s
+        # from the arena in fresh processes, against 6.70-6.75 TB/s with one
+        # allocation per buffer; offsetting the buffers against each other
+        # (4 KiB to 32 MiB) changed nothing.
         per_shard = [(self.S, torch.float16)] * w.n_d + [(self.S, torch.float32)] * 6
         arena = _Arena(self.device, per_shard * len(self.shard_ids))
         self._arena = arena
