@@ -84,6 +84,32 @@ def workload(args):
     return w
 
 
+def arm_config(args, w, elems: int, bytes_step: int, world: int) -> dict:
+    """The workload description both arms print (the reference arm times a
+    bounded sample of this same workload and says so in its cpu_baseline)."""
+    return {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
+            "bytes_per_param": round(bytes_step / max(elems, 1), 4), "bytes_per_step": bytes_step,
+            "storage": "fp16 grads and params, fp32 master/m/v (ping-pong)",
+            "math": ("ZS_MATH_FAST: u by corrected hardware reciprocal (within 1 ulp), all else IEEE; "
+                     "m/v bit-exact" if args.math == "fast" else "ZS_MATH_IEEE: every fp32 operation IEEE, "
+                     "bit-exact"),
+            "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
+            if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def shard_elements(w) -> int:
+    """Parameters one step updates (the rank's shard, or every shard), from
+    the oracle's partition (host arithmetic, as the library's)."""
+    import oracle
+    oracle.build()
+    lay = oracle.layout(list(w.numels), w.n_d, w.align)
+    s = int(lay["shard_numel"])
+    psi = int(lay["psi"])
+    valid = [max(0, min(s, psi - r * s)) for r in range(w.n_d)]
+    return valid[w.rank] if w.rank is not None else sum(valid)
+
+
 def workload_label(w, n_valid):
     return (f"{w.name}: Psi={w.psi:,} ({len(w.numels)} tensors), N_d={w.n_d}, "
             f"rank {w.rank} shard of {n_valid:,} params, fp16 grads x{w.n_d} + fp32 master/m/v")
@@ -251,6 +277,7 @@ def reference_arm(args, rank: int):
     if rank != 0:
         return
     w = workload(args)
+    elems = shard_elements(w)
     threads = os.cpu_count() or 1
     n_sample = min(4_000_000, max(w.psi // w.n_d, 1))
     per_step_s = max(0.5, min(5.0, 60.0 / max(args.steps + args.warmup, 1)))
@@ -270,7 +297,7 @@ def reference_arm(args, rank: int):
             "n_gpus": args.gpus, "steps": len(vals), "warmup": args.warmup,
             "ms_per_step": round(n_sample / (value * 1e9) * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": workload_label(w, n_sample), "parallelism": "host threads"},
+            "config": arm_config(args, w, elems, (26 + 2 * w.n_d) * elems, args.gpus),
             "cpu_baseline": {"value": round(value, 4), "unit": "Gparams/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "Gparams/s", "h2d_bytes_per_step": 0,
@@ -464,15 +491,7 @@ def main():
         "ms_per_step": round(ms_max / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
-                   "bytes_per_param": round(bytes_step / max(elems, 1), 4), "bytes_per_step": bytes_step,
-                   "storage": "fp16 grads and params, fp32 master/m/v (ping-pong)",
-                   "math": ("ZS_MATH_FAST: u by corrected hardware reciprocal (within 1 ulp), all else IEEE; "
-                            "m/v bit-exact" if args.math == "fast" else "ZS_MATH_IEEE: every fp32 operation IEEE, "
-                            "bit-exact"),
-                   "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
-                   if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": arm_config(args, w, elems, bytes_step, world),
         "hbm_gbs": round(hbm_gbs, 1),
         "pct_of_nominal_8tbs": round(100 * hbm_gbs / NOMINAL_HBM_GBS, 2),
         f"pct_of_{peak_kind}_peak": round(100 * hbm_gbs / peak, 2),
