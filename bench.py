@@ -372,8 +372,7 @@ def main():
         if not clip:
             if ev is not None:
                 ev[0].record(stream)
-            for i in range(len(run.views)):
-                run.reduce_adam(i)
+            run.reduce_adam_all()   # the fused kernels of every stepped shard (grouped launches)
             if ev is not None:
                 ev[1].record(stream)
         else:

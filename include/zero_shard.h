@@ -238,14 +238,17 @@ ZS_API double zero_state_bytes(double psi, int32_t n_d, int32_t stage, double k)
 /* ------------------------------------------------------------------------ */
 
 /* One optimizer step over n_shards shards, with a host round trip.
- * For every element j < n of every shard, in one fused kernel per shard:
+ * For every element j < n of every shard, in the fused kernels (consecutive
+ * shards of one access width share a launch; see
+ * zero_shard_reduce_adam_all_async):
  *   gs   = sum over k = 0..n_d-1, in that order, of fp32(grads[k][j])
  *   g    = gs * (float)(1 / (n_d * loss_scale))
  *   m'   = b1 m + (1 - b1) g;   v' = b2 v + (1 - b2) g^2
  *   u    = (m' / (1 - beta1^step)) / (sqrt(v' / (1 - beta2^step)) + eps)
  *   th'  = th - lr (u + weight_decay th);   params[j] = fp16_rn(th')
- * reading state set `cur`, writing set `cur ^ 1`; every fp32 operation is one
- * IEEE round-to-nearest step, no fused multiply-add.
+ * reading state set `cur`, writing set `cur ^ 1`; with ZS_MATH_IEEE every fp32
+ * operation is one IEEE round-to-nearest step, no fused multiply-add (see
+ * zs_adam.math for ZS_MATH_FAST).
  * The non-finite test of gs over all shards is ORed into *flag_dev (DEVICE
  * int32 scratch, cleared by this call).  The call then waits for the stream;
  * on overflow it rewrites every shard's params from master[cur] so the fp16
@@ -291,8 +294,8 @@ ZS_API int32_t zero_ctrl_init(zs_ctrl* ctrl_dev, double loss_scale, void* stream
 
 /* The same step with no host synchronisation (CUDA-graph friendly): the loss
  * scale, t and the ping-pong set come from *ctrl_dev, and the commit-or-skip
- * decision runs on the device.  Enqueues one fused kernel per shard with
- * n > 0 (zero_shard_reduce_adam_async) and then one commit kernel
+ * decision runs on the device.  Enqueues the fused kernels of every shard
+ * with n > 0 (zero_shard_reduce_adam_all_async) and then one commit kernel
  * (zero_step_commit_async). */
 ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                      const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream);
@@ -304,6 +307,17 @@ ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, i
  * zero_step_commit_async for all of them. */
 ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
                                             zs_ctrl* ctrl_dev, void* stream);
+
+/* The first half of zero_shard_step_async for every listed shard: the fused
+ * kernels only, without the commit (zero_step_commit_async follows).  Shards
+ * that share an access width, carry no qwZ copy and have n_d <= 64 are stepped
+ * up to 16 at a time by one launch of a grouped kernel that walks their
+ * concatenated elements (one launch ramp and tail instead of one per shard);
+ * the others get one launch each, as zero_shard_reduce_adam_async.  The
+ * arithmetic per element is the same in both.  Arguments and errors as
+ * zero_shard_step_async. */
+ZS_API int32_t zero_shard_reduce_adam_all_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                                const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream);
 
 /* Second half: if ctrl->overflow is set, rewrite every listed shard's params
  * from master[ctrl->cur] and halve the loss scale (floor 1), counting a skip;

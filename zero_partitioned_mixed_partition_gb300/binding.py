@@ -83,6 +83,7 @@ _SIGNATURES = {
     "zero_shard_step_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "zero_shard_step_host": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "zero_shard_reduce_adam_async": (_I32, [_P, _I32, _P, _P, _P]),
+    "zero_shard_reduce_adam_all_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "zero_shard_grad_sqnorm_async": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "zero_shard_clipped_adam_async": (_I32, [_P, _I32, _P, _F64, _P, _P, _P, _P]),
     "zero_shard_step_clipped_async": (_I32, [_P, _I32, _I32, _P, _F64, _P, _P, _P, _P]),
@@ -328,6 +329,14 @@ def zero_shard_step_async(shards: Sequence[ShardView], n_d: int, hp: Adam, ctrl_
     rc = lib().zero_shard_step_async(arr, len(shards), int(n_d), ctypes.byref(hp),
                                      _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
     _check(rc, "zero_shard_step_async")
+
+
+def zero_shard_reduce_adam_all_async(shards: Sequence[ShardView], n_d: int, hp: Adam, ctrl_dev: torch.Tensor,
+                                     stream=None):
+    arr = _shard_array(shards)
+    rc = lib().zero_shard_reduce_adam_all_async(arr, len(shards), int(n_d), ctypes.byref(hp),
+                                                _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_reduce_adam_all_async")
 
 
 class HostShardView(ShardView):

@@ -130,6 +130,10 @@ class WorkloadRunner:
     def reduce_adam(self, i: int = 0):
         binding.zero_shard_reduce_adam_async(self.views[i], self.w.n_d, self.hp, self.ctrl, stream=self.stream)
 
+    def reduce_adam_all(self):
+        """The fused kernels of every stepped shard (grouped launches), no commit."""
+        binding.zero_shard_reduce_adam_all_async(self.views, self.w.n_d, self.hp, self.ctrl, stream=self.stream)
+
     def commit(self):
         binding.zero_step_commit_async(self.views, self.hp, self.ctrl, stream=self.stream)
 
