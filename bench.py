@@ -496,7 +496,7 @@ def main():
         f"pct_of_{peak_kind}_peak": round(100 * hbm_gbs / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "shard_step_kernel", "peak_kind": peak_kind,
+                     "kernel": "group_step_kernel" if len(run.views) > 1 else "shard_step_kernel", "peak_kind": peak_kind,
                      "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_min": round(min(kern_ms), 5)},
         "clocks": clocks,
         "gpu_launches": int(launches),
