@@ -75,9 +75,12 @@ def test_sgd_step_matches_oracle(zs, oracle, cuda_device, n, n_d):
         _compare(run, r, ref, f"n={n} n_d={n_d} step {step}")
 
 
-def test_sgd_multi_shard(zs, oracle, cuda_device):
+@pytest.mark.parametrize("n_d", [8, 16, 20])
+def test_sgd_multi_shard(zs, oracle, cuda_device, n_d):
+    """Every shard of a ragged tensor list in one step: grouped launches (up to
+    16 shards each; 20 shards make a group of 16 and one of 4)."""
     numels = tuple(synth.ragged_numels(60, seed=4, max_exp=11))
-    w = _workload(0, 8, numels=numels, rank=None, align=128, grads_fresh_per_step=False, seed=9)
+    w = _workload(0, n_d, numels=numels, rank=None, align=128, grads_fresh_per_step=False, seed=9)
     run = WorkloadRunner(w, cuda_device)
     refs = {r: OracleSgd(oracle, to_np(run.state[r][0][0][: run.n_valid[r]])) for r in run.shard_ids}
     hp = zs.sgd(LR, MU, WD)

@@ -41,17 +41,19 @@ struct SgdArgs {
     int32_t* flag;        // &ctrl->overflow
 };
 
+// VEC elements of one shard starting at element e (grads / n_d: its
+// contribution table; params, n: its fp16 slice and length).
 template <int CAP, int VEC, int ND>
-__device__ __forceinline__ uint32_t sgd_elements(const SgdArgs<CAP>& p, float inv, float lr, float mu, float wd,
-                                                 int64_t e, const float* th_in, const float* b_in,
-                                                 float* th_out, float* b_out) {
+__device__ __forceinline__ uint32_t sgd_elements(const uint16_t* const (&grads)[CAP], int32_t n_d, uint16_t* params,
+                                                 int64_t n, float inv, float lr, float mu, float wd, int64_t e,
+                                                 const float* th_in, const float* b_in, float* th_out, float* b_out) {
     float th[VEC], b[VEC], acc[VEC];
-    if (!ZS_RANGE_OK(kSiteSgd, e, VEC, p.n)) return 0u;
+    if (!ZS_RANGE_OK(kSiteSgd, e, VEC, n)) return 0u;
     Mem<VEC>::load_f(th_in + e, th);
     Mem<VEC>::load_f(b_in + e, b);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
-    sum_contributions<CAP, VEC, ND>(p.grads, p.n_d, e, acc);
+    sum_contributions<CAP, VEC, ND>(grads, n_d, e, acc);
     uint32_t bad = 0;
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
@@ -63,7 +65,7 @@ __device__ __forceinline__ uint32_t sgd_elements(const SgdArgs<CAP>& p, float in
     }
     Mem<VEC>::store_f(th_out + e, th);
     Mem<VEC>::store_f(b_out + e, b);
-    Mem<VEC>::store_h(p.params + e, th);
+    Mem<VEC>::store_h(params + e, th);
     return bad;
 }
 
@@ -87,12 +89,120 @@ __global__ void __launch_bounds__(sgd_threads<VEC, CAP>()) sgd_step_kernel(const
     const int64_t nvec = p.n / VEC;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
-        bad |= sgd_elements<CAP, VEC, ND>(p, inv, lr, mu, wd, i * VEC, th_in, b_in, th_out, b_out);
+        bad |= sgd_elements<CAP, VEC, ND>(p.grads, p.n_d, p.params, p.n, inv, lr, mu, wd, i * VEC, th_in, b_in, th_out,
+                                          b_out);
     if (VEC > 1) {
         const int64_t e = nvec * VEC + threadIdx.x;
-        if (blockIdx.x == 0 && e < p.n) bad |= sgd_elements<CAP, 1, ND>(p, inv, lr, mu, wd, e, th_in, b_in, th_out, b_out);
+        if (blockIdx.x == 0 && e < p.n)
+            bad |= sgd_elements<CAP, 1, ND>(p.grads, p.n_d, p.params, p.n, inv, lr, mu, wd, e, th_in, b_in, th_out, b_out);
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
+}
+
+// Several shards of one step in one launch, as the Adam step's grouped kernel:
+// the grid walks the shards' concatenated vectors with a forward-only shard
+// cursor; each shard's tail is taken by one block.
+constexpr int kSgdGroupMax = 16;
+
+template <int CAP>
+struct SgdGroupArgs {
+    const uint16_t* grads[kSgdGroupMax][CAP];
+    float* master[kSgdGroupMax][2];
+    float* mom[kSgdGroupMax][2];
+    uint16_t* params[kSgdGroupMax];
+    int64_t n[kSgdGroupMax];
+    int64_t vstart[kSgdGroupMax + 1];
+    int32_t n_shards;
+    int32_t n_d;
+    double lr, momentum, weight_decay;
+    const zs_ctrl* ctrl;
+    int32_t* flag;
+};
+
+template <int CAP, int VEC, int ND>
+__global__ void __launch_bounds__(sgd_threads<VEC, CAP>())
+sgd_group_kernel(const __grid_constant__ SgdGroupArgs<CAP> a) {
+    __shared__ float s_inv;
+    __shared__ int s_cur;
+    if (threadIdx.x == 0) {
+        s_inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)a.n_d, a.ctrl->loss_scale)));
+        s_cur = a.ctrl->cur;
+    }
+    __syncthreads();
+    const float inv = s_inv;
+    const int cur = s_cur;
+    const float lr = __double2float_rn(a.lr), mu = __double2float_rn(a.momentum), wd = __double2float_rn(a.weight_decay);
+    uint32_t bad = 0;
+    const int64_t total = a.vstart[a.n_shards];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int s = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        while (i >= a.vstart[s + 1]) ++s;
+        bad |= sgd_elements<CAP, VEC, ND>(a.grads[s], a.n_d, a.params[s], a.n[s], inv, lr, mu, wd,
+                                          (i - a.vstart[s]) * VEC, a.master[s][cur], a.mom[s][cur],
+                                          a.master[s][cur ^ 1], a.mom[s][cur ^ 1]);
+    }
+    if (VEC > 1) {
+        for (int t = blockIdx.x; t < a.n_shards; t += gridDim.x) {
+            const int64_t e = a.n[t] / VEC * VEC + threadIdx.x;
+            if (e < a.n[t])
+                bad |= sgd_elements<CAP, 1, ND>(a.grads[t], a.n_d, a.params[t], a.n[t], inv, lr, mu, wd, e,
+                                                a.master[t][cur], a.mom[t][cur], a.master[t][cur ^ 1],
+                                                a.mom[t][cur ^ 1]);
+        }
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.flag, 1);
+}
+
+template <int CAP, int ND>
+int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl,
+                         cudaStream_t stream) {
+    SgdGroupArgs<CAP> a;
+    const bool wide = width == 2 && n_d > 4;
+    const int vec = wide ? 16 : 8;
+    a.vstart[0] = 0;
+    for (int g = 0; g < kSgdGroupMax; ++g) {
+        const bool on = g < count;
+        const bool live = on && shards[g].n > 0;   // an empty shard's table may be NULL
+        for (int k = 0; k < CAP; ++k) a.grads[g][k] = live && k < n_d ? shards[g].grads[k] : nullptr;
+        for (int i = 0; i < 2; ++i) {
+            a.master[g][i] = on ? shards[g].master[i] : nullptr;
+            a.mom[g][i] = on ? shards[g].m[i] : nullptr;
+        }
+        a.params[g] = on ? shards[g].params : nullptr;
+        a.n[g] = on ? shards[g].n : 0;
+        if (on) a.vstart[g + 1] = a.vstart[g] + shards[g].n / vec;
+    }
+    for (int g = count + 1; g <= kSgdGroupMax; ++g) a.vstart[g] = a.vstart[count];
+    a.n_shards = count;
+    a.n_d = n_d;
+    a.lr = hp.lr;
+    a.momentum = hp.momentum;
+    a.weight_decay = hp.weight_decay;
+    a.ctrl = ctrl;
+    a.flag = &ctrl->overflow;
+    auto go = [&](auto kernel, int threads) {
+        const int blocks = zs::persistent_blocks((const void*)kernel, threads, a.vstart[count] > 0 ? a.vstart[count] : 1);
+        kernel<<<blocks, threads, 0, stream>>>(a);
+        return zs::check_launch("sgd_group_kernel");
+    };
+    if constexpr (ND == 0 || ND > 4) {
+        if (wide) return go(sgd_group_kernel<CAP, 16, ND>, sgd_threads<16, CAP>());
+    }
+    return go(sgd_group_kernel<CAP, 8, ND>, sgd_threads<8, CAP>());
+}
+
+int32_t launch_group(const zs_shard* shards, int count, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl,
+                     cudaStream_t stream) {
+    switch (n_d) {
+    case 16: return launch_group_cap<16, 16>(shards, count, n_d, width, hp, ctrl, stream);
+    case 32: return launch_group_cap<32, 32>(shards, count, n_d, width, hp, ctrl, stream);
+    case 64: return launch_group_cap<64, 64>(shards, count, n_d, width, hp, ctrl, stream);
+    default: break;
+    }
+    if (n_d <= 4) return launch_group_cap<4, 0>(shards, count, n_d, width, hp, ctrl, stream);
+    if (n_d <= 16) return launch_group_cap<16, 0>(shards, count, n_d, width, hp, ctrl, stream);
+    return launch_group_cap<64, 0>(shards, count, n_d, width, hp, ctrl, stream);
 }
 
 template <int CAP, int VEC, int ND>
@@ -197,10 +307,18 @@ ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shard
         if (rc != ZS_OK) return rc;
     }
     cudaStream_t st = (cudaStream_t)stream;
-    for (int32_t i = 0; i < n_shards; ++i) {
-        if (shards[i].n == 0) continue;
-        int32_t rc = launch(shards[i], n_d, width[i], *hp, ctrl_dev, st);
+    // consecutive shards with one vector width: up to 16 per grouped launch
+    int32_t i = 0;
+    while (i < n_shards) {
+        if (shards[i].n == 0) { ++i; continue; }
+        const bool groupable = n_d <= 64 && width[i] >= 1;
+        int32_t j = i + 1;
+        if (groupable)
+            while (j < n_shards && j - i < kSgdGroupMax && width[j] == width[i]) ++j;
+        int32_t rc = (groupable && j - i > 1) ? launch_group(shards + i, j - i, n_d, width[i], *hp, ctrl_dev, st)
+                                              : launch(shards[i], n_d, width[i], *hp, ctrl_dev, st);
         if (rc != ZS_OK) return rc;
+        i = groupable ? j : i + 1;
     }
     const zs_adam no_adam{hp->lr, 0.0, 0.0, 0.0, 0.0};  // the commit's beta^t are unused by SGD
     return zs::launch_commit(shards, n_shards, no_adam, ctrl_dev, st);
