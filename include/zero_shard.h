@@ -196,7 +196,9 @@ typedef struct zs_ctrl {
  * n_d in [1, ZS_MAX_ND]; align a power of two.  Returns ZS_ERR_ARG for a bad
  * argument, a negative numel, or frag_cap smaller than the count (in which
  * case *n_frags_out holds the count needed and frags is left partly filled).
- * Runs on the host; no CUDA call. */
+ * Runs on the host; no CUDA call.
+ * Source: "DeepSpeed ZeRO Stages", sec. 2 (disjoint near-equal partition of the index set) and sec.
+ * 3.2 (flat contiguous gradient buffer). */
 ZS_API int32_t zero_partition_layout(const int64_t* numels, int32_t n_tensors, int32_t n_d,
                                      int32_t align, int64_t* psi_out, int64_t* psi_padded_out,
                                      int64_t* shard_numel_out, int64_t* tensor_offsets,
@@ -216,7 +218,8 @@ ZS_API int32_t zero_partition_layout(const int64_t* numels, int32_t n_tensors, i
  *                                  (frag_cap >= n_tensors + n_d - 1 always
  *                                  suffices).
  * The results are bit-identical to zero_partition_layout.  Host-side checks
- * return ZS_ERR_ARG / ZS_ERR_ALIGN (8-byte alignment) before any launch. */
+ * return ZS_ERR_ARG / ZS_ERR_ALIGN (8-byte alignment) before any launch.
+ * Source: "DeepSpeed ZeRO Stages", sec. 2 and sec. 3.2 (as zero_partition_layout). */
 ZS_API int32_t zero_partition_layout_device(const int64_t* numels_dev, int32_t n_tensors,
                                             int32_t n_d, int32_t align, int64_t* scalars_dev,
                                             int64_t* tensor_offsets_dev, int64_t* shard_offsets_dev,
@@ -230,7 +233,9 @@ ZS_API int32_t zero_partition_layout_device(const int64_t* numels_dev, int32_t n
  * optimizer multiplier k (12 for mixed-precision Adam):
  *   stage 0: (4 + k) psi          stage 1: 4 psi + k psi / n_d
  *   stage 2: 2 psi + (2 + k) psi / n_d      stage 3: (4 + k) psi / n_d
- * Returns NaN for a stage outside 0..3 or n_d < 1.  Host only. */
+ * Returns NaN for a stage outside 0..3 or n_d < 1.  Host only.
+ * Source: "DeepSpeed ZeRO Stages", sec. 1.2 and 3.1-3.3; "DeepSpeed ZeRO: Extreme Memory
+ * Efficiency", "Three stages of partitioning the redundancy away". */
 ZS_API double zero_state_bytes(double psi, int32_t n_d, int32_t stage, double k);
 
 /* ------------------------------------------------------------------------ */
@@ -255,7 +260,9 @@ ZS_API double zero_state_bytes(double psi, int32_t n_d, int32_t stage, double k)
  * slice again matches the committed state.  *overflow_out (HOST) gets 0 or 1.
  * The caller commits: overflow == 0 -> cur ^= 1, step + 1 for the next call;
  * overflow == 1 -> keep cur and step, halve the loss scale (floor 1).
- * step >= 1 is the Adam time t of this update (committed updates + 1). */
+ * step >= 1 is the Adam time t of this update (committed updates + 1).
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
+ * 2.1, Fact 1; skip and loss-scale halving: the dynamic loss-scale rule (not in the pages). */
 ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
                                int32_t* flag_dev, void* stream, int32_t* overflow_out);
@@ -283,20 +290,26 @@ ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t
  *   - every call shares the array, and it keeps the last call's contents; each
  *     call clears the words it uses before its kernels run.  Calls whose work
  *     overlaps on the GPU (other streams, other host threads) race on it, so
- *     order them. */
+ *     order them.
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
+ * 2.1, Fact 1 (the entry point itself has no counterpart in the pages). */
 ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                        const zs_adam* hp, double loss_scale, int64_t step,
                                        int32_t cur, void* stream, int32_t* overflow_out);
 
 /* Set up a device control block: loss scale L, t = 0, cur = 0, counters 0.
- * Stream-ordered (one tiny kernel). */
+ * Stream-ordered (one tiny kernel).
+ * Source: the dynamic loss-scale rule (not in the pages) and the Adam time t of "DeepSpeed ZeRO
+ * Stages", sec. 2.1, Fact 1. */
 ZS_API int32_t zero_ctrl_init(zs_ctrl* ctrl_dev, double loss_scale, void* stream);
 
 /* The same step with no host synchronisation (CUDA-graph friendly): the loss
  * scale, t and the ping-pong set come from *ctrl_dev, and the commit-or-skip
  * decision runs on the device.  Enqueues the fused kernels of every shard
  * with n > 0 (zero_shard_reduce_adam_all_async) and then one commit kernel
- * (zero_step_commit_async). */
+ * (zero_step_commit_async).
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
+ * 2.1, Fact 1. */
 ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                      const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream);
 
@@ -304,7 +317,9 @@ ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, i
  * non-finite test + Adam + fp16 cast kernel, with t = ctrl->step + 1, the
  * loss scale ctrl->loss_scale and set ctrl->cur; ORs its test into
  * ctrl->overflow.  Several shards of one step each get one call, then one
- * zero_step_commit_async for all of them. */
+ * zero_step_commit_async for all of them.
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
+ * 2.1, Fact 1. */
 ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
                                             zs_ctrl* ctrl_dev, void* stream);
 
@@ -315,7 +330,9 @@ ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, 
  * concatenated elements (one launch ramp and tail instead of one per shard);
  * the others get one launch each, as zero_shard_reduce_adam_async.  The
  * arithmetic per element is the same in both.  Arguments and errors as
- * zero_shard_step_async. */
+ * zero_shard_step_async.
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
+ * 2.1, Fact 1. */
 ZS_API int32_t zero_shard_reduce_adam_all_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                                 const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream);
 
@@ -323,7 +340,9 @@ ZS_API int32_t zero_shard_reduce_adam_all_async(const zs_shard* shards, int32_t 
  * from master[ctrl->cur] and halve the loss scale (floor 1), counting a skip;
  * otherwise flip ctrl->cur, advance t and beta^t.  Records last_overflow and
  * clears overflow for the next step.  The shard list must be the shards the
- * step updated (grads are not used). */
+ * step updated (grads are not used).
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beat 3 (the fp16 copy of the kept master);
+ * skip and halving: the dynamic loss-scale rule (not in the pages). */
 ZS_API int32_t zero_step_commit_async(const zs_shard* shards, int32_t n_shards, const zs_adam* hp,
                                       zs_ctrl* ctrl_dev, void* stream);
 
@@ -338,7 +357,9 @@ ZS_API int32_t zero_step_commit_async(const zs_shard* shards, int32_t n_shards, 
  * zero_shard_step_async, and the call waits for the stream and returns the
  * step's overflow flag in *overflow_out (HOST).  A host pointer that is not
  * page-locked and mapped for the current device returns ZS_ERR_ARG before any
- * launch. */
+ * launch.
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
+ * 2.1, Fact 1; host-resident data as in ZeRO-Offload, "DeepSpeed ZeRO Stages", sec. 5.1. */
 ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
                                     zs_ctrl* ctrl_dev, void* stream, int32_t* overflow_out);
 
@@ -365,7 +386,9 @@ ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs
  *   4. zero_step_commit_async for all the shards.
  * Per element: 4 n_d + 26 bytes without g_dev, 2 n_d + 34 with it; keep g
  * once n_d > 4.  Loss scale, t and the ping-pong set come from *ctrl_dev as in
- * zero_shard_step_async. */
+ * zero_shard_step_async.
+ * Source: "DeepSpeed ZeRO Stages", sec. 2.1, Fact 1 (clipping couples the coordinates through ||g||
+ * over all of P), with the update of "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3. */
 ZS_API int32_t zero_shard_grad_sqnorm_async(const zs_shard* shard, int32_t n_d, float* g_dev,
                                             double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
 ZS_API int32_t zero_shard_clipped_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
@@ -374,13 +397,16 @@ ZS_API int32_t zero_shard_clipped_adam_async(const zs_shard* shard, int32_t n_d,
 /* Steps 1-4 for shards that all live on this device (the norm is then exact
  * over them): clears *sqnorm_dev, runs pass 1 over every shard, pass 2 over
  * every shard, and the commit.  g_dev: HOST array of n_shards DEVICE
- * pointers (each may be NULL), or NULL to re-reduce everywhere. */
+ * pointers (each may be NULL), or NULL to re-reduce everywhere.
+ * Source: "DeepSpeed ZeRO Stages", sec. 2.1, Fact 1 (clipping). */
 ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                              const zs_adam* hp, double max_norm, float* const* g_dev,
                                              double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
 
 /* params[j] = fp16_rn(master[j]) for j < n (DEVICE buffers): initialises the
- * fp16 parameter slice from fp32 master weights.  Stream-ordered. */
+ * fp16 parameter slice from fp32 master weights.  Stream-ordered.
+ * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beat 3 (fp16 parameters cast from the fp32
+ * master). */
 ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params_dev, int64_t n,
                                        void* stream);
 
@@ -395,7 +421,8 @@ ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params
  * The momentum b lives in zs_shard.m (both sets; b starts at 0), zs_shard.v
  * is unused (may be NULL) and qcodes must be NULL.  Loss scale and the
  * ping-pong set come from *ctrl_dev; one fused kernel per shard, then the
- * device commit.  Per element 2 n_d + 18 bytes. */
+ * device commit.  Per element 2 n_d + 18 bytes.
+ * Source: "DeepSpeed ZeRO Stages", sec. 1.2 (mixed-precision SGD with momentum, K = 4). */
 ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                          const zs_sgd* hp, zs_ctrl* ctrl_dev, void* stream);
 
@@ -408,7 +435,8 @@ ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shard
  * params; no qwZ copy), run on n_threads host threads (0 = all cores).  Same
  * arithmetic, ping-pong, overflow test and restore as zero_shard_step, bit for
  * bit; synchronous; *overflow_out (HOST) gets 0 or 1 and the caller commits as
- * for zero_shard_step.  No CUDA call. */
+ * for zero_shard_step.  No CUDA call.
+ * Source: "DeepSpeed ZeRO Stages", sec. 5.1 (ZeRO-Offload: the optimizer step on the CPU). */
 ZS_API int32_t zero_shard_step_cpu(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                    const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
                                    int32_t n_threads, int32_t* overflow_out);
@@ -418,11 +446,15 @@ ZS_API int32_t zero_shard_step_cpu(const zs_shard* shards, int32_t n_shards, int
 /* ------------------------------------------------------------------------ */
 
 /* codes / scales (DEVICE) of n fp16 params (DEVICE), by the rule of
- * zs_shard.qcodes.  Stream-ordered. */
+ * zs_shard.qcodes.  Stream-ordered.
+ * Source: "ZeRO Optimization: Stages 1, 2, and 3 Explained" (ZeRO++ quantized weights); "DeepSpeed
+ * ZeRO Stages", sec. 5.3. */
 ZS_API int32_t zero_qwz_quantize(const uint16_t* params_dev, int64_t n, int8_t* codes_dev,
                                  float* scales_dev, void* stream);
 /* The all-gather receiver's side: params[j] = fp16_rn(codes[j] * scales[j / 256])
- * (DEVICE buffers).  Stream-ordered. */
+ * (DEVICE buffers).  Stream-ordered.
+ * Source: "ZeRO Optimization: Stages 1, 2, and 3 Explained" (ZeRO++ quantized weights); "DeepSpeed
+ * ZeRO Stages", sec. 5.3. */
 ZS_API int32_t zero_qwz_dequantize(const int8_t* codes_dev, const float* scales_dev, int64_t n,
                                    uint16_t* params_dev, void* stream);
 
@@ -430,11 +462,14 @@ ZS_API int32_t zero_qwz_dequantize(const int8_t* codes_dev, const float* scales_
 /* Diagnostics.                                                              */
 /* ------------------------------------------------------------------------ */
 
-/* Static description of a status code. */
+/* Static description of a status code.
+ * Source: no counterpart in the pages (a property of this library). */
 ZS_API const char* zero_status_string(int32_t status);
-/* Text of the last ZS_ERR_CUDA failure on the calling host thread ("" if none). */
+/* Text of the last ZS_ERR_CUDA failure on the calling host thread ("" if none).
+ * Source: no counterpart in the pages (a property of this library). */
 ZS_API const char* zero_last_error(void);
-/* Number of kernels this library has enqueued in this process. */
+/* Number of kernels this library has enqueued in this process.
+ * Source: no counterpart in the pages (a property of this library). */
 ZS_API int64_t zero_kernel_launches(void);
 
 /* Index checks of the debug build.  The same sources compiled with
@@ -446,7 +481,8 @@ ZS_API int64_t zero_kernel_launches(void);
  * device, writes that record (0: none) to *first_fault, clears it, and
  * returns 1 in the checked build; the ordinary build has no checks and
  * returns 0 with *first_fault = 0.  ZS_ERR_ARG if first_fault is NULL,
- * ZS_ERR_CUDA if the record cannot be read. */
+ * ZS_ERR_CUDA if the record cannot be read.
+ * Source: no counterpart in the pages (a property of this library). */
 ZS_API int32_t zero_debug_checks(uint64_t* first_fault);
 
 #ifdef __cplusplus
