@@ -88,7 +88,9 @@
 /* ------------------------------------------------------------------------ */
 
 /* Decode one binary16 value: 1 sign bit, 5 exponent bits (bias 15), 10
- * fraction bits.  Exact: every binary16 value is a binary32 value. */
+ * fraction bits.  Exact: every binary16 value is a binary32 value.  (The fp16
+ * gradients and parameters of "ZeRO Stage 1 Math", "The 16-bytes-per-parameter
+ * budget".) */
 float oracle_f16_to_f32(uint16_t h)
 {
     int sign = (h >> 15) & 1;
@@ -105,7 +107,8 @@ float oracle_f16_to_f32(uint16_t h)
     return sign ? -mag : mag;
 }
 
-/* Round one binary32 value to binary16, ties to even. */
+/* Round one binary32 value to binary16, ties to even (the fp16 cast of "ZeRO
+ * Stage 1 Math", "The per-step mechanics", beat 3). */
 uint16_t oracle_f32_to_f16(float x)
 {
     uint16_t sign = signbit(x) ? 0x8000 : 0;
@@ -314,7 +317,9 @@ int32_t oracle_adam_apply(const float* g, int64_t n, float* master, float* m, fl
 
 /* One whole shard step: reduce, test, and update only when every reduced
  * gradient is finite.  On overflow nothing is written and *overflow = 1.
- * scratch must hold n floats. */
+ * scratch must hold n floats.  ("ZeRO Stage 1 Math", "The per-step
+ * mechanics", beats 2-3; the skip is the dynamic loss-scale rule, which the
+ * pages do not describe.) */
 int32_t oracle_shard_step(const uint16_t* const* contrib, int32_t n_d, int64_t n,
                           float* master, float* m, float* v, uint16_t* params,
                           double lr, double beta1, double beta2, double eps,
@@ -334,7 +339,9 @@ int32_t oracle_shard_step(const uint16_t* const* contrib, int32_t n_d, int64_t n
 /* Bookkeeping after the overflow test of one step (over every shard stepped):
  * overflow -> the step is skipped, the loss scale halves (never below 1) and
  * the Adam time does not advance; otherwise the update is committed and the
- * count of applied updates grows by one. */
+ * count of applied updates grows by one.  (The usual dynamic loss-scale rule;
+ * the pages do not describe loss scaling.  The Adam time t is the one of the
+ * bias correction, "DeepSpeed ZeRO Stages", sec. 2.1, Fact 1.) */
 void oracle_commit(int32_t overflow, double* loss_scale, int64_t* applied_steps)
 {
     if (overflow) {
@@ -362,7 +369,8 @@ void oracle_grad_sqnorm(const float* g, int64_t n, double* sqnorm)
 
 /* Clip factor for a global squared norm: min(1, max_norm / (||g|| + 1e-6)),
  * formed in double and rounded once to float.  max_norm <= 0 disables
- * clipping (factor 1). */
+ * clipping (factor 1).  ("DeepSpeed ZeRO Stages", sec. 2.1, Fact 1 names the
+ * clipping; the formula is the common one, the pages give none.) */
 float oracle_clip_factor(double sqnorm, double max_norm)
 {
     if (!(max_norm > 0.0)) return 1.0f;
@@ -371,7 +379,8 @@ float oracle_clip_factor(double sqnorm, double max_norm)
     return (float)c;
 }
 
-/* g_j <- g_j * c in fp32. */
+/* g_j <- g_j * c in fp32 (the clipped gradient; "DeepSpeed ZeRO Stages",
+ * sec. 2.1, Fact 1). */
 void oracle_scale(float* g, int64_t n, float c)
 {
     for (int64_t j = 0; j < n; ++j) g[j] = g[j] * c;
@@ -410,7 +419,9 @@ void oracle_qwz_quantize(const uint16_t* params, int64_t n, int8_t* codes, float
     }
 }
 
-/* The receiver's side: params[j] = fp16(q_j * scale_of_its_block). */
+/* The receiver's side of the quantized all-gather: params[j] =
+ * fp16(q_j * scale_of_its_block) ("ZeRO Optimization: Stages 1, 2, and 3
+ * Explained", ZeRO++ quantized weights). */
 void oracle_qwz_dequantize(const int8_t* codes, const float* scales, int64_t n, uint16_t* params)
 {
     for (int64_t j = 0; j < n; ++j)
