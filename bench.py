@@ -581,14 +581,16 @@ def end_to_end(args, run, stream, dev, world):
         step()
     torch.cuda.synchronize()
     ms = zdist.max_over_ranks((time.perf_counter() - t0) * 1e3, device=dev)
-    val = run.elements_per_step() * world * args.e2e_steps / (ms / 1e3) / 1e9
+    # the end-to-end step covers one shard (the first stepped one) per rank
+    val = n * world * args.e2e_steps / (ms / 1e3) / 1e9
     path = ("zero_shard_step_host: contributions read from and fp16 shard written to pinned host memory "
             "by the fused kernel (NVLink-C2C), device commit, flag returned"
             if args.e2e_mode == "mapped" else
             "pinned host grads -> device (cudaMemcpyAsync), zero_shard_step_async, fp16 shard + control block "
             "-> pinned host")
     return {"value": round(val, 3), "unit": "Gparams/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / args.e2e_steps, 4), "mode": args.e2e_mode, "path": path}
+            "ms_per_step": round(ms / args.e2e_steps, 4), "mode": args.e2e_mode, "path": path,
+            "shard_params": n}
 
 
 if __name__ == "__main__":
