@@ -566,7 +566,7 @@ def end_to_end(args, run, stream, dev, world):
             with torch.cuda.stream(stream):
                 for h, g in zip(host_grads, run.grads[r]):
                     g[:n].copy_(h, non_blocking=True)
-                run.step()
+                binding.zero_shard_step_async([run.views[0]], run.w.n_d, run.hp, run.ctrl, stream=stream)
                 host_params.copy_(run.state[r][3][:n], non_blocking=True)
                 host_ctrl.copy_(run.ctrl, non_blocking=True)
             stream.synchronize()
