@@ -451,7 +451,8 @@ def main():
         with open(path, "w") as f:
             for k, ms in enumerate(kern_ms):
                 gbs = bytes_step / (ms / 1e3) / 1e9
-                f.write(json.dumps({"workload": w.name, "n_d": w.n_d, "rank": rank, "t": t_first + k,
+                f.write(json.dumps({"workload": w.name, "n_d": w.n_d, "process_rank": rank,
+                                    "shard": w.rank if w.rank is not None else "all", "t": t_first + k,
                                     "overflow": 0, "loss_scale": ctrl["loss_scale"], "kernel_ms": round(ms, 5),
                                     "gparams_s": round(elems / (ms / 1e3) / 1e9, 3), "kernel_gbs": round(gbs, 1),
                                     "pct_of_peak": round(100 * gbs / peak_gbs, 2)}) + "\n")
@@ -504,7 +505,7 @@ def main():
     }
     if args.optimizer == "sgd":
         line["optimizer"] = {"kind": "sgd", "momentum": 0.9, "timed": "fused kernel + commit"}
-        line["roofline"]["kernel"] = "sgd_step_kernel + commit_kernel"
+        line["roofline"]["kernel"] = ("sgd_group_kernel" if len(run.views) > 1 else "sgd_step_kernel") + " + commit_kernel"
     if args.qwz:
         line["qwz"] = {"block": 256, "extra_bytes_per_param": round(1 + 4 / 256, 4)}
     if clip_info is not None:
