@@ -380,14 +380,12 @@ def main():
                 run.sqnorm.zero_()
             if ev is not None:
                 ev[0].record(stream)
-            for i, view in enumerate(run.views):
-                binding.zero_shard_grad_sqnorm_async(view, w.n_d, run.sqnorm, run.ctrl,
-                                                     g_dev=run.gbuf[i] if run.gbuf else None, stream=stream)
+            binding.zero_shard_grad_sqnorm_all_async(run.views, w.n_d, run.sqnorm, run.ctrl,
+                                                     g_dev=run.gbuf if run.gbuf else None, stream=stream)
             if ev is not None:
                 ev[2].record(stream)
-            for i, view in enumerate(run.views):
-                binding.zero_shard_clipped_adam_async(view, w.n_d, run.hp, args.clip, run.sqnorm, run.ctrl,
-                                                      g_dev=run.gbuf[i] if run.gbuf else None, stream=stream)
+            binding.zero_shard_clipped_adam_all_async(run.views, w.n_d, run.hp, args.clip, run.sqnorm, run.ctrl,
+                                                      g_dev=run.gbuf if run.gbuf else None, stream=stream)
             if ev is not None:
                 ev[1].record(stream)
         run.commit()

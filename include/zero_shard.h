@@ -394,6 +394,20 @@ ZS_API int32_t zero_shard_grad_sqnorm_async(const zs_shard* shard, int32_t n_d, 
 ZS_API int32_t zero_shard_clipped_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
                                              double max_norm, const float* g_dev,
                                              const double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
+
+/* Passes 1 and 3 above for a list of shards: consecutive shards of one access
+ * width go up to 16 at a time into one launch that walks their concatenated
+ * elements (n_d <= 64; one shard per launch above).  g_dev: HOST array of
+ * n_shards DEVICE pointers (entries may be NULL), or NULL for none.  The
+ * arithmetic per element is that of the one-shard calls.
+ * Source: "DeepSpeed ZeRO Stages", sec. 2.1, Fact 1 (clipping), with the update of "ZeRO Stage 1
+ *   Math", "The per-step mechanics", beats 2-3. */
+ZS_API int32_t zero_shard_grad_sqnorm_all_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                                float* const* g_dev, double* sqnorm_dev, zs_ctrl* ctrl_dev,
+                                                void* stream);
+ZS_API int32_t zero_shard_clipped_adam_all_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                                 const zs_adam* hp, double max_norm, float* const* g_dev,
+                                                 const double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
 /* Steps 1-4 for shards that all live on this device (the norm is then exact
  * over them): clears *sqnorm_dev, runs pass 1 over every shard, pass 2 over
  * every shard, and the commit.  g_dev: HOST array of n_shards DEVICE

@@ -123,3 +123,48 @@ def test_sync_step_uses_groups(zs, oracle, cuda_device):
     oracle_group_step(oracle, refs, host, w, w.loss_scale, 0)
     for (master, m, v, params), ref in zip(state, refs):
         ref.compare(to_np(master[1]), to_np(m[1]), to_np(v[1]), f16_bits(params))
+
+
+@pytest.mark.parametrize("keep_g", [False, True])
+@pytest.mark.parametrize("case", ["ragged_like", "cut_runs", "over_16"])
+def test_grouped_clip_passes_equal_per_shard(zs, cuda_device, case, keep_g):
+    """Both clipping passes over a shard list (grouped launches) give the same
+    flags, squared norm (to the rounding of the double additions) and bits as
+    one launch per shard."""
+    n_d, sizes, misaligned, qwz = CASES[case]
+    w = _workload(n_d, seed=3 * len(sizes) + n_d)
+    hp = zs.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, math=zs.ZS_MATH_FAST)
+    va, sa, _ = _make(zs, cuda_device, w, sizes, misaligned, qwz)
+    vb, sb, _ = _make(zs, cuda_device, w, sizes, misaligned, qwz)
+    ga = [torch.zeros(n + 16, dtype=torch.float32, device=cuda_device)[(1 if i in misaligned else 0):][:n]
+          for i, n in enumerate(sizes)] if keep_g else None
+    gb = [t.clone() for t in ga] if keep_g else None
+    ca, cb = zs.new_ctrl(cuda_device), zs.new_ctrl(cuda_device)
+    zs.zero_ctrl_init(ca, w.loss_scale)
+    zs.zero_ctrl_init(cb, w.loss_scale)
+    sqa = torch.zeros(1, dtype=torch.float64, device=cuda_device)
+    sqb = torch.zeros(1, dtype=torch.float64, device=cuda_device)
+    for step in range(1, 3):
+        sqa.zero_(); sqb.zero_()
+        zs.zero_shard_grad_sqnorm_all_async(va, n_d, sqa, ca, g_dev=ga)
+        for i, v in enumerate(vb):
+            zs.zero_shard_grad_sqnorm_async(v, n_d, sqb, cb, g_dev=gb[i] if gb else None)
+        torch.cuda.synchronize()
+        a, b = float(sqa.item()), float(sqb.item())
+        assert abs(a - b) <= 1e-12 * max(b, 1e-300), (a, b)
+        sqa.copy_(sqb)                          # the same clip factor on both sides
+        max_norm = 0.5 * np.sqrt(b)
+        zs.zero_shard_clipped_adam_all_async(va, n_d, hp, max_norm, sqa, ca, g_dev=ga)
+        for i, v in enumerate(vb):
+            zs.zero_shard_clipped_adam_async(v, n_d, hp, max_norm, sqb, cb, g_dev=gb[i] if gb else None)
+        zs.zero_step_commit_async(va, hp, ca)
+        zs.zero_step_commit_async(vb, hp, cb)
+        torch.cuda.synchronize()
+        assert zs.read_ctrl(ca) == zs.read_ctrl(cb)
+        cur = zs.read_ctrl(ca)["cur"]
+        for i, ((ma, mma, vva, pa), (mb, mmb, vvb, pb)) in enumerate(zip(sa, sb)):
+            for x, y in ((ma[cur], mb[cur]), (mma[cur], mmb[cur]), (vva[cur], vvb[cur])):
+                assert torch.equal(x.view(torch.int32), y.view(torch.int32)), f"{case} shard {i} step {step}"
+            assert torch.equal(pa.view(torch.int16), pb.view(torch.int16)), f"{case} shard {i} step {step}"
+        for i in qwz:
+            assert torch.equal(va[i].qcodes, vb[i].qcodes)

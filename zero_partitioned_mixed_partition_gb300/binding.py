@@ -87,6 +87,8 @@ _SIGNATURES = {
     "zero_shard_grad_sqnorm_async": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "zero_shard_clipped_adam_async": (_I32, [_P, _I32, _P, _F64, _P, _P, _P, _P]),
     "zero_shard_step_clipped_async": (_I32, [_P, _I32, _I32, _P, _F64, _P, _P, _P, _P]),
+    "zero_shard_grad_sqnorm_all_async": (_I32, [_P, _I32, _I32, _P, _P, _P, _P]),
+    "zero_shard_clipped_adam_all_async": (_I32, [_P, _I32, _I32, _P, _F64, _P, _P, _P, _P]),
     "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
     "zero_shard_step_cpu": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _I32, _P]),
@@ -466,6 +468,33 @@ def zero_shard_step_clipped_async(shards: Sequence[ShardView], n_d: int, hp: Ada
                                              _dev_ptr(sqnorm_dev, torch.float64, "sqnorm_dev"),
                                              _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
     _check(rc, "zero_shard_step_clipped_async")
+
+
+def _g_table(shards, g_dev):
+    if g_dev is None:
+        return None
+    return (_P * len(shards))(*[_dev_ptr(g, torch.float32, "g_dev") for g in g_dev])
+
+
+def zero_shard_grad_sqnorm_all_async(shards: Sequence[ShardView], n_d: int, sqnorm_dev: torch.Tensor,
+                                     ctrl_dev: torch.Tensor, g_dev=None, stream=None):
+    """Clipping pass 1 for a list of shards (grouped launches)."""
+    arr = _shard_array(shards)
+    rc = lib().zero_shard_grad_sqnorm_all_async(arr, len(shards), int(n_d), _g_table(shards, g_dev),
+                                                _dev_ptr(sqnorm_dev, torch.float64, "sqnorm_dev"),
+                                                _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_grad_sqnorm_all_async")
+
+
+def zero_shard_clipped_adam_all_async(shards: Sequence[ShardView], n_d: int, hp: Adam, max_norm: float,
+                                      sqnorm_dev: torch.Tensor, ctrl_dev: torch.Tensor, g_dev=None, stream=None):
+    """Clipping pass 2 for a list of shards (grouped launches)."""
+    arr = _shard_array(shards)
+    rc = lib().zero_shard_clipped_adam_all_async(arr, len(shards), int(n_d), ctypes.byref(hp), float(max_norm),
+                                                 _g_table(shards, g_dev),
+                                                 _dev_ptr(sqnorm_dev, torch.float64, "sqnorm_dev"),
+                                                 _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_clipped_adam_all_async")
 
 
 def zero_params_from_master(master: torch.Tensor, params: torch.Tensor, n: int, stream=None):

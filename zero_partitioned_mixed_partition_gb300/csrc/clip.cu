@@ -27,17 +27,26 @@ namespace {
 
 constexpr int kClipThreads = 256;
 
+// Shards per launch: up to 16 consecutive shards of one access width share a
+// launch (their pointer tables travel in the parameter block; 1 for the
+// 1024-contribution table, which alone fills it).
+template <int CAP>
+constexpr int clip_group() { return CAP <= 64 ? 16 : 1; }
+
 template <int CAP>
 struct ClipArgs {
-    const uint16_t* grads[CAP];
-    float* master[2];
-    float* m[2];
-    float* v[2];
-    uint16_t* params;
-    float* g;             // pass 1 writes / pass 2 reads it; nullptr: re-reduce
+    static constexpr int G = clip_group<CAP>();
+    const uint16_t* grads[G][CAP];
+    float* master[G][2];
+    float* m[G][2];
+    float* v[G][2];
+    uint16_t* params[G];
+    float* g[G];          // pass 1 writes / pass 2 reads it; nullptr: re-reduce
+    int64_t n[G];
+    int64_t vstart[G + 1];  // first vector of each shard in the launch's index space
+    int32_t n_shards;
     double* sqnorm;       // pass 1 adds to it, pass 2 reads it
     double max_norm;
-    int64_t n;
     int32_t n_d;
     zs_adam hp;
     const zs_ctrl* ctrl;  // loss scale, t and the ping-pong set
@@ -61,13 +70,14 @@ __device__ double block_sum(double x) {
     return x;
 }
 
-// g_j for VEC elements from the contributions; returns the non-finite test.
+// g_j for VEC elements of shard s from its contributions; returns the
+// non-finite test.
 template <int CAP, int VEC, int ND>
-__device__ __forceinline__ uint32_t reduced_grad(const ClipArgs<CAP>& p, float inv, int64_t e, float* g) {
+__device__ __forceinline__ uint32_t reduced_grad(const ClipArgs<CAP>& p, int s, float inv, int64_t e, float* g) {
     float acc[VEC];
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
-    sum_contributions<CAP, VEC, ND>(p.grads, p.n_d, e, acc);
+    sum_contributions<CAP, VEC, ND>(p.grads[s], p.n_d, e, acc);
     uint32_t bad = 0;
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
@@ -100,16 +110,21 @@ __device__ __forceinline__ double sum_squares(const float* g) {
 }
 
 template <int CAP, int VEC, int ND>
-__device__ __forceinline__ uint32_t norm_elements(const ClipArgs<CAP>& p, float inv, int64_t e, double& sq) {
+__device__ __forceinline__ uint32_t norm_elements(const ClipArgs<CAP>& p, int s, float inv, int64_t e, double& sq) {
     float g[VEC];
-    if (!ZS_RANGE_OK(kSiteNorm, e, VEC, p.n)) return 0u;
-    const uint32_t bad = reduced_grad<CAP, VEC, ND>(p, inv, e, g);
+    if (!ZS_RANGE_OK(kSiteNorm, e, VEC, p.n[s])) return 0u;
+    const uint32_t bad = reduced_grad<CAP, VEC, ND>(p, s, inv, e, g);
     sq = __dadd_rn(sq, sum_squares<VEC>(g));
-    if (p.g != nullptr) Mem<VEC>::store_f(p.g + e, g);
+    if (p.g[s] != nullptr) Mem<VEC>::store_f(p.g[s] + e, g);
     return bad;
 }
 
-// Pass 1: non-finite test and sum of squares of the shard's reduced gradient.
+// Both passes walk the launch's shards as one index space: vector i belongs
+// to the shard s with vstart[s] <= i < vstart[s + 1]; the index only grows, so
+// each thread's shard cursor only moves forward.  Each shard's tail (fewer
+// than VEC elements) is taken by one block.
+
+// Pass 1: non-finite test and sum of squares of the shards' reduced gradient.
 template <int CAP, int VEC, int ND>
 __global__ void __launch_bounds__(kClipThreads) grad_norm_kernel(const __grid_constant__ ClipArgs<CAP> p) {
     __shared__ float s_inv;
@@ -119,22 +134,31 @@ __global__ void __launch_bounds__(kClipThreads) grad_norm_kernel(const __grid_co
     const float inv = s_inv;
     double sq = 0.0;
     uint32_t bad = 0;
-    const int64_t nvec = p.n / VEC;
+    const int64_t total = p.vstart[p.n_shards];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
-        bad |= norm_elements<CAP, VEC, ND>(p, inv, i * VEC, sq);
+    int s = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        while (i >= p.vstart[s + 1]) ++s;
+        bad |= norm_elements<CAP, VEC, ND>(p, s, inv, (i - p.vstart[s]) * VEC, sq);
+    }
     if (VEC > 1) {
-        const int64_t e = nvec * VEC + threadIdx.x;
-        if (blockIdx.x == 0 && e < p.n) bad |= norm_elements<CAP, 1, ND>(p, inv, e, sq);
+        for (int t = blockIdx.x; t < p.n_shards; t += gridDim.x) {
+            const int64_t e = p.n[t] / VEC * VEC + threadIdx.x;
+            if (e < p.n[t]) bad |= norm_elements<CAP, 1, ND>(p, t, inv, e, sq);
+        }
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
-    const double total = block_sum(sq);
-    if (threadIdx.x == 0) atomicAdd(p.sqnorm, total);
+    const double total_sq = block_sum(sq);
+    if (threadIdx.x == 0) atomicAdd(p.sqnorm, total_sq);
 }
 
 // Pass 2: clipped Adam / AdamW update and fp16 cast.  FAST: ZS_MATH_FAST.
+// The 8-element variant is held to 64 registers: four blocks per SM, as the
+// unclipped step's 8-element kernel (the shard cursor would otherwise take it
+// to 68 registers and three blocks).
 template <int CAP, int VEC, int ND, bool FAST>
-__global__ void __launch_bounds__(kClipThreads) clipped_step_kernel(const __grid_constant__ ClipArgs<CAP> p) {
+__global__ void __launch_bounds__(kClipThreads, VEC == 8 ? 4 : 0)
+clipped_step_kernel(const __grid_constant__ ClipArgs<CAP> p) {
     __shared__ Coef s_coef;
     __shared__ float s_clip;
     __shared__ int s_cur;
@@ -156,36 +180,35 @@ __global__ void __launch_bounds__(kClipThreads) clipped_step_kernel(const __grid
     const Coef c = s_coef;
     const float clip = s_clip;
     const int cur = s_cur;
-    const float* th_in = p.master[cur];
-    const float* m_in = p.m[cur];
-    const float* v_in = p.v[cur];
-    float* th_out = p.master[cur ^ 1];
-    float* m_out = p.m[cur ^ 1];
-    float* v_out = p.v[cur ^ 1];
 
-    auto step = [&](auto vec_tag, int64_t e) {
+    auto step = [&](auto vec_tag, int s, int64_t e) {
         constexpr int V = decltype(vec_tag)::value;
         float th[V], m[V], v[V], g[V];
-        if (!ZS_RANGE_OK(kSiteClipped, e, V, p.n)) return;
-        Mem<V>::load_f(th_in + e, th);
-        Mem<V>::load_f(m_in + e, m);
-        Mem<V>::load_f(v_in + e, v);
-        if (p.g != nullptr) Mem<V>::load_f(p.g + e, g);
-        else reduced_grad<CAP, V, ND>(p, c.inv, e, g);
+        if (!ZS_RANGE_OK(kSiteClipped, e, V, p.n[s])) return;
+        Mem<V>::load_f(p.master[s][cur] + e, th);
+        Mem<V>::load_f(p.m[s][cur] + e, m);
+        Mem<V>::load_f(p.v[s][cur] + e, v);
+        if (p.g[s] != nullptr) Mem<V>::load_f(p.g[s] + e, g);
+        else reduced_grad<CAP, V, ND>(p, s, c.inv, e, g);
 #pragma unroll
         for (int j = 0; j < V; ++j) adam_apply<FAST>(c, __fmul_rn(g[j], clip), th[j], m[j], v[j]);
-        Mem<V>::store_f(th_out + e, th);
-        Mem<V>::store_f(m_out + e, m);
-        Mem<V>::store_f(v_out + e, v);
-        Mem<V>::store_h(p.params + e, th);
+        Mem<V>::store_f(p.master[s][cur ^ 1] + e, th);
+        Mem<V>::store_f(p.m[s][cur ^ 1] + e, m);
+        Mem<V>::store_f(p.v[s][cur ^ 1] + e, v);
+        Mem<V>::store_h(p.params[s] + e, th);
     };
-    const int64_t nvec = p.n / VEC;
+    const int64_t total = p.vstart[p.n_shards];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
-        step(std::integral_constant<int, VEC>{}, i * VEC);
+    int s = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        while (i >= p.vstart[s + 1]) ++s;
+        step(std::integral_constant<int, VEC>{}, s, (i - p.vstart[s]) * VEC);
+    }
     if (VEC > 1) {
-        const int64_t e = nvec * VEC + threadIdx.x;
-        if (blockIdx.x == 0 && e < p.n) step(std::integral_constant<int, 1>{}, e);
+        for (int t = blockIdx.x; t < p.n_shards; t += gridDim.x) {
+            const int64_t e = p.n[t] / VEC * VEC + threadIdx.x;
+            if (e < p.n[t]) step(std::integral_constant<int, 1>{}, t, e);
+        }
     }
 }
 
@@ -197,7 +220,8 @@ template <int CAP, int VEC, int ND, bool FAST>
 int32_t launch_pass_as(Pass pass, const ClipArgs<CAP>& a, cudaStream_t stream) {
     const void* k = pass == Pass::Norm ? (const void*)grad_norm_kernel<CAP, VEC, ND>
                                        : (const void*)clipped_step_kernel<CAP, VEC, ND, FAST>;
-    const int blocks = zs::persistent_blocks(k, kClipThreads, a.n / VEC > 0 ? a.n / VEC : 1);
+    const int64_t work = a.vstart[a.n_shards];
+    const int blocks = zs::persistent_blocks(k, kClipThreads, work > 0 ? work : 1);
     if (pass == Pass::Norm)
         grad_norm_kernel<CAP, VEC, ND><<<blocks, kClipThreads, 0, stream>>>(a);
     else
@@ -215,55 +239,90 @@ int32_t launch_pass(Pass pass, const ClipArgs<CAP>& a, cudaStream_t stream) {
     return launch_pass_as<CAP, VEC, ND, false>(pass, a, stream);
 }
 
+// One launch of pass 1 or 2 over shards[0, count) (count <= the group size),
+// all of access width `width`; g[i]: shard i's kept-g buffer or nullptr.
 template <int CAP, int ND>
-int32_t launch_cap(Pass pass, const zs_shard& s, int32_t n_d, int width, float* g, double* sqnorm,
-                   double max_norm, const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
-    ClipArgs<CAP> a;
-    for (int k = 0; k < CAP; ++k) a.grads[k] = k < n_d ? s.grads[k] : nullptr;
-    for (int i = 0; i < 2; ++i) {
-        a.master[i] = s.master[i];
-        a.m[i] = s.m[i];
-        a.v[i] = s.v[i];
+int32_t launch_cap(Pass pass, const zs_shard* shards, int count, int32_t n_d, int width, float* const* g,
+                   double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+    using Args = ClipArgs<CAP>;
+    Args a;
+    const bool wide = (ND == 0 || ND > 4) && width == 2 && n_d > 4;
+    const int vec = wide ? 16 : (width >= 1 ? 8 : 1);
+    a.vstart[0] = 0;
+    for (int q = 0; q < Args::G; ++q) {
+        const bool on = q < count;
+        const bool live = on && shards[q].n > 0;   // an empty shard's table may be NULL
+        for (int k = 0; k < CAP; ++k) a.grads[q][k] = live && k < n_d ? shards[q].grads[k] : nullptr;
+        for (int i = 0; i < 2; ++i) {
+            a.master[q][i] = on ? shards[q].master[i] : nullptr;
+            a.m[q][i] = on ? shards[q].m[i] : nullptr;
+            a.v[q][i] = on ? shards[q].v[i] : nullptr;
+        }
+        a.params[q] = on ? shards[q].params : nullptr;
+        a.g[q] = on && g != nullptr ? g[q] : nullptr;
+        a.n[q] = on ? shards[q].n : 0;
+        if (on) a.vstart[q + 1] = a.vstart[q] + shards[q].n / vec;
     }
-    a.params = s.params;
-    a.g = g;
+    for (int q = count + 1; q <= Args::G; ++q) a.vstart[q] = a.vstart[count];
+    a.n_shards = count;
     a.sqnorm = sqnorm;
     a.max_norm = max_norm;
-    a.n = s.n;
     a.n_d = n_d;
     a.hp = hp;
     a.ctrl = ctrl;
     a.flag = &ctrl->overflow;
     if constexpr (ND == 0 || ND > 4) {
-        if (width == 2 && n_d > 4) return launch_pass<CAP, 16, ND>(pass, a, stream);
+        if (wide) return launch_pass<CAP, 16, ND>(pass, a, stream);
     }
     if (width >= 1) return launch_pass<CAP, 8, ND>(pass, a, stream);
     return launch_pass<CAP, 1, ND>(pass, a, stream);
 }
 
-int32_t launch_by_nd(Pass pass, const zs_shard& s, int32_t n_d, int width, float* g, double* sqnorm,
-                     double max_norm, const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+// Largest number of shards one launch takes for this n_d.
+int group_size(int32_t n_d) { return n_d <= 64 ? clip_group<64>() : clip_group<ZS_MAX_ND>(); }
+
+int32_t launch_by_nd(Pass pass, const zs_shard* shards, int count, int32_t n_d, int width, float* const* g,
+                     double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
     switch (n_d) {
-    case 16: return launch_cap<16, 16>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    case 32: return launch_cap<32, 32>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    case 64: return launch_cap<64, 64>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    case 16: return launch_cap<16, 16>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    case 32: return launch_cap<32, 32>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    case 64: return launch_cap<64, 64>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
     default: break;
     }
-    if (n_d <= 4) return launch_cap<4, 0>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    if (n_d <= 16) return launch_cap<16, 0>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    if (n_d <= 64) return launch_cap<64, 0>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    return launch_cap<ZS_MAX_ND, 0>(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    if (n_d <= 4) return launch_cap<4, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    if (n_d <= 16) return launch_cap<16, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    if (n_d <= 64) return launch_cap<64, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    return launch_cap<ZS_MAX_ND, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
 }
 
-// Pass 1 or 2 for one shard; after pass 2 the shard's qwZ copy (if any) is
-// rebuilt from the new fp16 slice in its own pass (3 + 4/256 bytes per element).
-int32_t launch(Pass pass, const zs_shard& s, int32_t n_d, int width, float* g, double* sqnorm, double max_norm,
-               const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
-    int32_t rc = launch_by_nd(pass, s, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    if (rc == ZS_OK && pass == Pass::Update && s.qcodes != nullptr)
-        rc = zs::launch_qwz(nullptr, s.params, s.n, s.qcodes, s.qscales, 0, (s.n + kQwzBlock - 1) / kQwzBlock,
-                            stream);
-    return rc;
+// Pass 1 or 2 for shards[0, n_shards): consecutive non-empty shards of one
+// access width share a launch (up to the group size); after pass 2 each
+// shard's qwZ copy (if any) is rebuilt from its new fp16 slice in its own pass
+// (3 + 4/256 bytes per element).
+int32_t launch_all(Pass pass, const zs_shard* shards, int32_t n_shards, int32_t n_d, const int* width,
+                   float* const* g, double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl,
+                   cudaStream_t stream) {
+    const int gmax = group_size(n_d);
+    int32_t i = 0;
+    while (i < n_shards) {
+        if (shards[i].n == 0) { ++i; continue; }
+        int32_t j = i + 1;
+        while (j < n_shards && j - i < gmax && width[j] == width[i] && shards[j].n > 0) ++j;
+        int32_t rc = launch_by_nd(pass, shards + i, j - i, n_d, width[i], g ? g + i : nullptr, sqnorm, max_norm, hp,
+                                  ctrl, stream);
+        if (rc != ZS_OK) return rc;
+        if (pass == Pass::Update) {
+            for (int32_t k = i; k < j; ++k) {
+                const zs_shard& s = shards[k];
+                if (s.qcodes == nullptr) continue;
+                rc = zs::launch_qwz(nullptr, s.params, s.n, s.qcodes, s.qscales, 0, (s.n + kQwzBlock - 1) / kQwzBlock,
+                                    stream);
+                if (rc != ZS_OK) return rc;
+            }
+        }
+        i = j;
+    }
+    return ZS_OK;
 }
 
 // Width allowed by the shard together with its kept-g buffer (fp32 like the state).
@@ -276,6 +335,20 @@ int32_t check_with_g(const zs_shard& s, int32_t n_d, const float* g, int* width)
     return ZS_OK;
 }
 
+// Argument checks shared by the entry points; *width gets each shard's width.
+int32_t check_list(const zs_shard* shards, int32_t n_shards, int32_t n_d, float* const* g, const double* sqnorm,
+                   const zs_ctrl* ctrl, int* width) {
+    if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS || n_d < 1 || n_d > ZS_MAX_ND ||
+        sqnorm == nullptr || ctrl == nullptr)
+        return ZS_ERR_ARG;
+    if (!zs::aligned_to(sqnorm, 8) || !zs::aligned_to(ctrl, 8)) return ZS_ERR_ALIGN;
+    for (int32_t i = 0; i < n_shards; ++i) {
+        int32_t rc = check_with_g(shards[i], n_d, g ? g[i] : nullptr, &width[i]);
+        if (rc != ZS_OK) return rc;
+    }
+    return ZS_OK;
+}
+
 }  // namespace
 
 namespace zs {
@@ -284,64 +357,58 @@ uint64_t take_fault_clip() { return take_fault(); }
 
 extern "C" {
 
+ZS_API int32_t zero_shard_grad_sqnorm_all_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                                float* const* g_dev, double* sqnorm_dev, zs_ctrl* ctrl_dev,
+                                                void* stream) {
+    int width[ZS_MAX_SHARDS];
+    int32_t rc = check_list(shards, n_shards, n_d, g_dev, sqnorm_dev, ctrl_dev, width);
+    if (rc != ZS_OK) return rc;
+    const zs_adam none{0.0, 0.0, 0.0, 0.0, 0.0, 0, 0};
+    return launch_all(Pass::Norm, shards, n_shards, n_d, width, g_dev, sqnorm_dev, 0.0, none, ctrl_dev,
+                      (cudaStream_t)stream);
+}
+
+ZS_API int32_t zero_shard_clipped_adam_all_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
+                                                 const zs_adam* hp, double max_norm, float* const* g_dev,
+                                                 const double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream) {
+    if (!zs::valid_hp(hp) || !(max_norm == max_norm)) return ZS_ERR_ARG;
+    int width[ZS_MAX_SHARDS];
+    int32_t rc = check_list(shards, n_shards, n_d, g_dev, sqnorm_dev, ctrl_dev, width);
+    if (rc != ZS_OK) return rc;
+    return launch_all(Pass::Update, shards, n_shards, n_d, width, g_dev, const_cast<double*>(sqnorm_dev), max_norm,
+                      *hp, ctrl_dev, (cudaStream_t)stream);
+}
+
 ZS_API int32_t zero_shard_grad_sqnorm_async(const zs_shard* shard, int32_t n_d, float* g_dev,
                                             double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream) {
-    if (shard == nullptr || n_d < 1 || n_d > ZS_MAX_ND || sqnorm_dev == nullptr || ctrl_dev == nullptr)
-        return ZS_ERR_ARG;
-    if (!zs::aligned_to(sqnorm_dev, 8) || !zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
-    int width = 0;
-    int32_t rc = check_with_g(*shard, n_d, g_dev, &width);
-    if (rc != ZS_OK) return rc;
-    if (shard->n == 0) return ZS_OK;
-    const zs_adam none{0.0, 0.0, 0.0, 0.0, 0.0};
-    return launch(Pass::Norm, *shard, n_d, width, g_dev, sqnorm_dev, 0.0, none, ctrl_dev, (cudaStream_t)stream);
+    float* const g[1] = {g_dev};
+    return zero_shard_grad_sqnorm_all_async(shard, 1, n_d, g_dev ? g : nullptr, sqnorm_dev, ctrl_dev, stream);
 }
 
 ZS_API int32_t zero_shard_clipped_adam_async(const zs_shard* shard, int32_t n_d, const zs_adam* hp,
                                              double max_norm, const float* g_dev, const double* sqnorm_dev,
                                              zs_ctrl* ctrl_dev, void* stream) {
-    if (shard == nullptr || n_d < 1 || n_d > ZS_MAX_ND || !zs::valid_hp(hp) || sqnorm_dev == nullptr ||
-        ctrl_dev == nullptr || !(max_norm == max_norm))
-        return ZS_ERR_ARG;
-    if (!zs::aligned_to(sqnorm_dev, 8) || !zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
-    int width = 0;
-    int32_t rc = check_with_g(*shard, n_d, g_dev, &width);
-    if (rc != ZS_OK) return rc;
-    if (shard->n == 0) return ZS_OK;
-    return launch(Pass::Update, *shard, n_d, width, const_cast<float*>(g_dev), const_cast<double*>(sqnorm_dev),
-                  max_norm, *hp, ctrl_dev, (cudaStream_t)stream);
+    float* const g[1] = {const_cast<float*>(g_dev)};
+    return zero_shard_clipped_adam_all_async(shard, 1, n_d, hp, max_norm, g_dev ? g : nullptr, sqnorm_dev,
+                                             ctrl_dev, stream);
 }
 
 ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                              const zs_adam* hp, double max_norm, float* const* g_dev,
                                              double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream) {
     zs::NvtxRange nvtx_range("zero_shard_step_clipped_async");
-    if (n_d < 1 || n_d > ZS_MAX_ND || !zs::valid_hp(hp) || sqnorm_dev == nullptr || ctrl_dev == nullptr ||
-        !(max_norm == max_norm))
-        return ZS_ERR_ARG;
-    if (!zs::aligned_to(sqnorm_dev, 8) || !zs::aligned_to(ctrl_dev, 8)) return ZS_ERR_ALIGN;
-    if (shards == nullptr || n_shards < 1 || n_shards > ZS_MAX_SHARDS) return ZS_ERR_ARG;
+    if (!zs::valid_hp(hp) || !(max_norm == max_norm)) return ZS_ERR_ARG;
     int width[ZS_MAX_SHARDS];
-    for (int32_t i = 0; i < n_shards; ++i) {
-        int32_t rc = check_with_g(shards[i], n_d, g_dev ? g_dev[i] : nullptr, &width[i]);
-        if (rc != ZS_OK) return rc;
-    }
+    int32_t rc = check_list(shards, n_shards, n_d, g_dev, sqnorm_dev, ctrl_dev, width);
+    if (rc != ZS_OK) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t err = cudaMemsetAsync(sqnorm_dev, 0, sizeof(double), st);
     if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_clipped_async: clear sqnorm");
-    const zs_adam none{0.0, 0.0, 0.0, 0.0, 0.0};
-    for (int32_t i = 0; i < n_shards; ++i) {
-        if (shards[i].n == 0) continue;
-        int32_t rc = launch(Pass::Norm, shards[i], n_d, width[i], g_dev ? g_dev[i] : nullptr, sqnorm_dev, 0.0,
-                            none, ctrl_dev, st);
-        if (rc != ZS_OK) return rc;
-    }
-    for (int32_t i = 0; i < n_shards; ++i) {
-        if (shards[i].n == 0) continue;
-        int32_t rc = launch(Pass::Update, shards[i], n_d, width[i], g_dev ? g_dev[i] : nullptr, sqnorm_dev,
-                            max_norm, *hp, ctrl_dev, st);
-        if (rc != ZS_OK) return rc;
-    }
+    const zs_adam none{0.0, 0.0, 0.0, 0.0, 0.0, 0, 0};
+    rc = launch_all(Pass::Norm, shards, n_shards, n_d, width, g_dev, sqnorm_dev, 0.0, none, ctrl_dev, st);
+    if (rc != ZS_OK) return rc;
+    rc = launch_all(Pass::Update, shards, n_shards, n_d, width, g_dev, sqnorm_dev, max_norm, *hp, ctrl_dev, st);
+    if (rc != ZS_OK) return rc;
     return zs::launch_commit(shards, n_shards, *hp, ctrl_dev, st);
 }
 
