@@ -324,11 +324,12 @@ ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, 
                                             zs_ctrl* ctrl_dev, void* stream);
 
 /* The first half of zero_shard_step_async for every listed shard: the fused
- * kernels only, without the commit (zero_step_commit_async follows).  Shards
- * that share an access width, carry no qwZ copy and have n_d <= 64 are stepped
- * up to 16 at a time by one launch of a grouped kernel that walks their
- * concatenated elements (one launch ramp and tail instead of one per shard);
- * the others get one launch each, as zero_shard_reduce_adam_async.  The
+ * kernels only, without the commit (zero_step_commit_async follows).
+ * Consecutive shards that share an access width and all carry (or all lack) a
+ * qwZ copy, with n_d <= 64, are stepped up to 16 at a time by one launch of a
+ * grouped kernel that walks their concatenated elements (one launch ramp and
+ * tail instead of one per shard); the others get one launch each, as
+ * zero_shard_reduce_adam_async.  The
  * arithmetic per element is the same in both.  Arguments and errors as
  * zero_shard_step_async.
  * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.

@@ -1,6 +1,6 @@
-"""Grouped launches: consecutive shards with one access width and no qwZ copy
-are stepped up to 16 at a time by one launch that walks their concatenated
-elements (zero_shard_reduce_adam_all_async, and inside zero_shard_step_async
+"""Grouped launches: consecutive shards with one access width (all with or
+all without a qwZ copy) are stepped up to 16 at a time by one launch that
+walks their concatenated elements (zero_shard_reduce_adam_all_async, and inside zero_shard_step_async
 and zero_shard_step).  The result must be bit-identical to one launch per
 shard (zero_shard_reduce_adam_async), and equal to the oracle, for groups cut
 by a misaligned shard, by a shard with a qwZ copy and by the 16-shard limit,
@@ -56,6 +56,8 @@ CASES = {
     "over_16": (4, [int(x) for x in np.random.Generator(np.random.PCG64(5)).integers(0, 3000, 37)], (), ()),
     "cut_runs": (8, [2048 * 3 + 5, 4096, 0, 2048 * 2 + 1, 777, 5000, 6, 3000, 2048 * 4], (3,), (6,)),
     "tiny_tails": (64, [1, 3, 15, 17, 33, 0, 250], (), ()),
+    "qwz_runs": (16, [5000, 256 * 20, 256 * 7 + 3, 1, 4099, 256 * 40, 3000], (), (0, 1, 2, 3, 4, 5)),
+    "qwz_narrow": (4, [256 * 33 + 17, 700, 256 * 8, 9000, 257], (), (0, 1, 2, 3, 4)),
 }
 
 
@@ -104,8 +106,10 @@ def test_grouped_equals_per_shard_and_oracle(zs, oracle, cuda_device, case, math
                 ref.compare(to_np(ma[cur]), to_np(mma[cur]), to_np(vva[cur]), f16_bits(pa),
                             what=f"{case} {math} shard {i} step {step}")
         for i in qwz:
-            codes, _ = oracle.qwz_quantize(f16_bits(sa[i][3]))
+            codes, scales = oracle.qwz_quantize(f16_bits(sa[i][3]))
             assert np.array_equal(to_np(va[i].qcodes[:sizes[i]]), codes)
+            assert np.array_equal(to_np(va[i].qscales[:scales.size]).view(np.uint32), scales.view(np.uint32))
+            assert torch.equal(va[i].qcodes, vb[i].qcodes)
 
 
 def test_sync_step_uses_groups(zs, oracle, cuda_device):

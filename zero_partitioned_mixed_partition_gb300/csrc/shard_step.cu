@@ -192,6 +192,8 @@ struct GroupArgs {
     float* v[kGroupMax][2];
     uint16_t* params[kGroupMax];
     int64_t n[kGroupMax];
+    int8_t* qcodes[kGroupMax];   // qwZ copies (QZ kernels only)
+    float* qscales[kGroupMax];
     int64_t vstart[kGroupMax + 1];
     int32_t n_shards;
     int32_t n_d;
@@ -209,9 +211,13 @@ struct GroupArgs {
 // Each thread keeps a cursor on its current shard; the index only grows, so
 // the cursor only moves forward.  Each shard's ragged tail (fewer than VEC
 // elements) is stepped by one block.  Arithmetic and order per element are
-// those of shard_step_kernel.
-template <int CAP, int VEC, int ND, bool FAST>
-__global__ void __launch_bounds__(kThreads) group_step_kernel(const __grid_constant__ GroupArgs<CAP> a) {
+// those of shard_step_kernel.  QZ (shards with a qwZ copy): every shard's
+// vector range starts on a warp boundary (vstart rounded up to 32), so the
+// lanes that hold one 256-parameter block always belong to one shard and
+// reduce its scale by shuffles, as in shard_step_kernel.
+template <int CAP, int VEC, int ND, bool QZ, bool FAST>
+__global__ void __launch_bounds__(kThreads, step_min_blocks<VEC, ND, QZ>())
+group_step_kernel(const __grid_constant__ GroupArgs<CAP> a) {
     __shared__ Coef s_coef;
     __shared__ int s_cur;
     if (threadIdx.x == 0) {
@@ -233,12 +239,40 @@ __global__ void __launch_bounds__(kThreads) group_step_kernel(const __grid_const
     const int64_t total = a.vstart[a.n_shards];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int s = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        while (i >= a.vstart[s + 1]) ++s;
-        float th[VEC];
-        bad |= step_elements<CAP, VEC, ND, FAST>(a.grads[s], a.n_d, a.params[s], a.n[s], c, (i - a.vstart[s]) * VEC,
-                                                 a.master[s][cur], a.m[s][cur], a.v[s][cur], a.master[s][cur ^ 1],
-                                                 a.m[s][cur ^ 1], a.v[s][cur ^ 1], th);
+    if constexpr (!QZ) {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+            while (i >= a.vstart[s + 1]) ++s;
+            float th[VEC];
+            bad |= step_elements<CAP, VEC, ND, FAST>(a.grads[s], a.n_d, a.params[s], a.n[s], c,
+                                                     (i - a.vstart[s]) * VEC, a.master[s][cur], a.m[s][cur],
+                                                     a.v[s][cur], a.master[s][cur ^ 1], a.m[s][cur ^ 1],
+                                                     a.v[s][cur ^ 1], th);
+        }
+    } else {
+        static_assert(VEC == 8 || VEC == 16, "qwZ needs the vector layouts");
+        constexpr int G = kQwzBlock / VEC;
+        const int lane = threadIdx.x & 31;
+        for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < total; i0 += stride) {
+            while (i0 >= a.vstart[s + 1]) ++s;        // the same shard for the whole warp
+            const int64_t w0 = i0 - a.vstart[s];      // warp's first vector in the shard, a multiple of 32
+            const int64_t li = w0 + lane;
+            const bool active = li < a.n[s] / VEC;
+            float th[VEC], x[VEC];
+            if (active)
+                bad |= step_elements<CAP, VEC, ND, FAST>(a.grads[s], a.n_d, a.params[s], a.n[s], c, li * VEC,
+                                                         a.master[s][cur], a.m[s][cur], a.v[s][cur],
+                                                         a.master[s][cur ^ 1], a.m[s][cur ^ 1], a.v[s][cur ^ 1], th);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) x[j] = active ? as_fp16_value(th[j]) : 0.0f;
+            int8_t q[VEC];
+            const float scale = qwz_group_codes<VEC, G>(x, active ? VEC : 0, q);
+            const int64_t block = (w0 + (lane & ~(G - 1))) * VEC / kQwzBlock;
+            if ((block + 1) * kQwzBlock <= a.n[s]) {  // full block: every lane of the group is active
+                if (ZS_RANGE_OK(kSiteQwzFused, li * VEC, VEC, a.n[s])) store_codes<VEC>(a.qcodes[s] + li * VEC, q);
+                if ((lane & (G - 1)) == 0 && ZS_RANGE_OK(kSiteScale, block, 1, (a.n[s] + kQwzBlock - 1) / kQwzBlock))
+                    a.qscales[s][block] = scale;
+            }
+        }
     }
     if (VEC > 1) {
         for (int t = blockIdx.x; t < a.n_shards; t += gridDim.x) {
@@ -718,6 +752,7 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
                          const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
     GroupArgs<CAP> a;
     const int vec = (width == 2 && n_d > 4) ? 16 : 8;
+    const bool qz = shards[0].qcodes != nullptr;   // all or none of the group
     a.vstart[0] = 0;
     for (int g = 0; g < kGroupMax; ++g) {
         const bool on = g < count;
@@ -730,7 +765,12 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
         }
         a.params[g] = on ? shards[g].params : nullptr;
         a.n[g] = on ? shards[g].n : 0;
-        if (g < count) a.vstart[g + 1] = a.vstart[g] + shards[g].n / vec;
+        a.qcodes[g] = on ? shards[g].qcodes : nullptr;
+        a.qscales[g] = on ? shards[g].qscales : nullptr;
+        if (g < count) {
+            const int64_t nv = shards[g].n / vec;
+            a.vstart[g + 1] = a.vstart[g] + (qz ? (nv + 31) / 32 * 32 : nv);   // warp-aligned for qwZ
+        }
     }
     for (int g = count + 1; g <= kGroupMax; ++g) a.vstart[g] = a.vstart[count];
     a.n_shards = count;
@@ -749,14 +789,16 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
     // the same kernel choice as for one shard (launch_step_cap / launch_math)
     if constexpr (ND == 0 || ND > 4) {
         if (vec == 16) {
+            if (qz) return go(group_step_kernel<CAP, 16, ND, true, false>);
             if constexpr (ND > 0) {
-                if (fast) return go(group_step_kernel<CAP, 16, ND, true>);
+                if (fast) return go(group_step_kernel<CAP, 16, ND, false, true>);
             }
-            return go(group_step_kernel<CAP, 16, ND, false>);
+            return go(group_step_kernel<CAP, 16, ND, false, false>);
         }
     }
-    if (fast) return go(group_step_kernel<CAP, 8, ND, true>);
-    return go(group_step_kernel<CAP, 8, ND, false>);
+    if (qz) return go(group_step_kernel<CAP, 8, ND, true, false>);
+    if (fast) return go(group_step_kernel<CAP, 8, ND, false, true>);
+    return go(group_step_kernel<CAP, 8, ND, false, false>);
 }
 
 int32_t launch_group(const zs_shard* shards, int count, int32_t n_d, int width, const Coef* coef, int32_t cur,
@@ -772,20 +814,23 @@ int32_t launch_group(const zs_shard* shards, int count, int32_t n_d, int width, 
     return launch_group_cap<64, 0>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, stream);
 }
 
-// The fused kernels of one step for shards[0, n_shards): consecutive shards
-// with the same vector width and no qwZ copy go up to kGroupMax per launch of
-// the grouped kernel (n_d <= 64); every other shard gets its own launch.
-// Empty shards launch nothing.
+// The fused kernels of one step for shards[0, n_shards): consecutive
+// non-empty shards with the same vector width, all with or all without a qwZ
+// copy, go up to kGroupMax per launch of the grouped kernel (n_d <= 64);
+// every other shard gets its own launch.  Empty shards launch nothing.
 int32_t launch_steps(const zs_shard* shards, int32_t n_shards, int32_t n_d, const int* width, const Coef* coef,
                      int32_t cur, const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
     int32_t i = 0;
     while (i < n_shards) {
         const zs_shard& s = shards[i];
         if (s.n == 0) { ++i; continue; }
-        const bool groupable = n_d <= 64 && width[i] >= 1 && s.qcodes == nullptr;
+        const bool groupable = n_d <= 64 && width[i] >= 1;
+        const bool qz = s.qcodes != nullptr;
         int32_t j = i + 1;
         if (groupable) {
-            while (j < n_shards && j - i < kGroupMax && width[j] == width[i] && shards[j].qcodes == nullptr) ++j;
+            while (j < n_shards && j - i < kGroupMax && width[j] == width[i] && (shards[j].qcodes != nullptr) == qz &&
+                   shards[j].n > 0)
+                ++j;
         }
         int32_t rc;
         if (groupable && j - i > 1) rc = launch_group(shards + i, j - i, n_d, width[i], coef, cur, hp, ctrl, flag, stream);
