@@ -277,3 +277,60 @@ def sgd_apply(g, master, mom, params, *, lr, momentum, weight_decay):
                                   weight_decay)
     if rc != 0:
         raise ValueError("oracle_sgd_apply: invalid arguments")
+
+
+# ----------------------------------------------------------- 8-bit Adam ---
+
+ADAM8_BLOCK = 2048
+
+
+def _lib_adam8():
+    lib = _load()
+    if not getattr(lib, "_adam8_typed", False):
+        lib.oracle_adam8_maps.argtypes = [_P, _P]
+        lib.oracle_adam8_maps.restype = None
+        lib.oracle_adam8_code_signed.argtypes = [ctypes.c_float, _P]
+        lib.oracle_adam8_code_signed.restype = ctypes.c_uint8
+        lib.oracle_adam8_code_unsigned.argtypes = [ctypes.c_float, _P]
+        lib.oracle_adam8_code_unsigned.restype = ctypes.c_uint8
+        lib.oracle_adam8_apply.argtypes = [_P, _I64, _P, _P, _P, _P, _P, _P, _F64, _F64, _F64, _F64, _F64, _I64]
+        lib.oracle_adam8_apply.restype = _I32
+        lib._adam8_typed = True
+    return lib
+
+
+def adam8_maps():
+    """The two code tables of 8-bit Adam: (mag7[128] signed-map magnitudes,
+    mag8[256] unsigned map), float32."""
+    mag7 = np.empty(128, np.float32)
+    mag8 = np.empty(256, np.float32)
+    _lib_adam8().oracle_adam8_maps(_ptr(mag7), _ptr(mag8))
+    return mag7, mag8
+
+
+def adam8_code_signed(x: float) -> int:
+    """Signed-map code of one float32 x in [-1, 1]."""
+    mag7, _ = adam8_maps()
+    return int(_lib_adam8().oracle_adam8_code_signed(ctypes.c_float(x), _ptr(mag7)))
+
+
+def adam8_code_unsigned(x: float) -> int:
+    """Unsigned-map code of one float32 x in [0, 1]."""
+    _, mag8 = adam8_maps()
+    return int(_lib_adam8().oracle_adam8_code_unsigned(ctypes.c_float(x), _ptr(mag8)))
+
+
+def adam8_apply(g, master, m_codes, v_codes, m_scale, v_scale, params, *, lr, beta1, beta2, eps, weight_decay,
+                step):
+    """In-place 8-bit Adam update of float32 master, uint8 codes, float32
+    per-2048 scales and uint16 params."""
+    g = _contig(g, np.float32)
+    for a, dt in ((master, np.float32), (m_codes, np.uint8), (v_codes, np.uint8), (m_scale, np.float32),
+                  (v_scale, np.float32)):
+        if a.dtype != dt or not a.flags.c_contiguous:
+            raise TypeError(f"expected contiguous {dt}")
+    rc = _lib_adam8().oracle_adam8_apply(_ptr(g), g.size, _ptr(master), _ptr(m_codes), _ptr(v_codes),
+                                         _ptr(m_scale), _ptr(v_scale), _ptr(params), lr, beta1, beta2, eps,
+                                         weight_decay, int(step))
+    if rc != 0:
+        raise ValueError("oracle_adam8_apply: invalid arguments")

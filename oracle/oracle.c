@@ -39,6 +39,11 @@
  *                        ("ZeRO Optimization: Stages 1, 2, and 3 Explained",
  *                         ZeRO++ quantized weights; "DeepSpeed ZeRO Stages"
  *                         sec. 5.3, qwZ)
+ *   oracle_adam8_maps,   8-bit Adam, the optimizer of K = 6 ("DeepSpeed ZeRO
+ *   oracle_adam8_apply   Stages" sec. 1.2): m and v kept as 8-bit codes of a
+ *                        dynamic map with a scale per block of 2048, after
+ *                        Dettmers et al., "8-bit Optimizers via Block-wise
+ *                        Quantization"
  *
  * Precision.  The pages fix the precisions: fp16 gradients and parameters,
  * fp32 master weights, m and v ("ZeRO Stage 1 Math", "The 16-bytes-per-
@@ -70,6 +75,11 @@
  *     the last one possibly shorter; scale = max|x| / 127 in fp32;
  *     q = rint(x / scale) (ties to even) in fp32, 0 when the scale is 0;
  *     the receiver rebuilds fp16(q * scale).
+ *   - 8-bit Adam (named with its K, nothing more): block-wise quantization of
+ *     m and v after Dettmers et al. (blocks of 2048, absmax scale, nearest
+ *     code of a decimal-exponent map, signed for m and unsigned for v, ties
+ *     to the smaller magnitude), fp32 master; the map's fraction values are
+ *     the upper ends of their steps so that x = 1 is exact;
  *
  * Parity pins for every function live in the tests (closed forms and worked
  * values printed on the pages, exhaustive fp16 checks against numpy, the
@@ -452,6 +462,152 @@ int32_t oracle_sgd_apply(const float* g, int64_t n, float* master, float* mom, u
         mom[j] = b;
         master[j] = th_new;
         if (params) params[j] = oracle_f32_to_f16(th_new);
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 8-bit Adam: m and v stored as 8-bit codes with a scale per block.         */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name "8-bit Adam" only through its state multiplier K = 6
+ * ("DeepSpeed ZeRO Stages" sec. 1.2): an fp32 master (4 bytes) and one byte
+ * each for m and v.  The method followed is the block-wise 8-bit Adam of
+ * Dettmers, Lewis, Shleifer and Zettlemoyer, "8-bit Optimizers via Block-wise
+ * Quantization" (ICLR 2022): the states are cut into blocks of 2048
+ * consecutive elements, each block keeps its largest magnitude as its scale,
+ * and every element keeps the code of the table value nearest to
+ * state / scale, the table being their dynamic (decimal-exponent) map.  Each
+ * step dequantizes, runs the fp32 Adam update and quantizes the new states
+ * again. */
+
+#define ORACLE_ADAM8_BLOCK 2048
+
+/* Value of code k (0 <= k < 2^bits) of the dynamic map over [0, 1]: code 0
+ * is 0; otherwise the run of leading zero bits of k in a field of `bits` bits
+ * is the decimal exponent E, the first set bit is the indicator, and the
+ * f bits below it (f = bits - E - 1) pick one of F = 2^f equal steps of the
+ * fraction range [0.1, 1]; the value is 10^-E * (0.1 + 0.9 (j + 1) / F) for
+ * those bits j, formed in double in that order and rounded once to float.
+ * (Reading: the fraction values are the upper ends of the F steps, so the
+ * block's largest magnitude, x = 1, is exact.) */
+static float oracle_dyn_value(int k, int bits)
+{
+    if (k == 0) return 0.0f;
+    int len = 0;
+    while ((k >> len) != 0) ++len;       /* bit length of k */
+    int e = bits - len;                  /* leading zeros: the decimal exponent */
+    int f = len - 1;                     /* fraction bits below the indicator */
+    int j = k - (1 << f);
+    double p10 = 1.0;
+    for (int i = 0; i < e; ++i) p10 = p10 * 10.0;
+    double frac = 0.1 + 0.9 * ((double)(j + 1) / (double)(1 << f));
+    return (float)(frac / p10);
+}
+
+/* The two code tables: mag7[128], the magnitudes of the signed map (a sign
+ * bit and 7 magnitude bits, for m), and mag8[256], the unsigned map (8 bits,
+ * for v >= 0). */
+void oracle_adam8_maps(float* mag7, float* mag8)
+{
+    for (int k = 0; k < 128; ++k) mag7[k] = oracle_dyn_value(k, 7);
+    for (int k = 0; k < 256; ++k) mag8[k] = oracle_dyn_value(k, 8);
+}
+
+/* Index of the table entry nearest to a (distances in double); of two
+ * equally near entries the smaller one.  A NaN a gives 0. */
+static int oracle_nearest(float a, const float* table, int count)
+{
+    int best = 0;
+    double best_d = fabs((double)a - (double)table[0]);
+    for (int k = 1; k < count; ++k) {
+        double d = fabs((double)a - (double)table[k]);
+        if (d < best_d) {
+            best = k;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* Code of x in [-1, 1] under the signed map: bit 7 set for x < 0 (unless the
+ * magnitude code is 0), bits 0-6 the code of |x| in mag7. */
+uint8_t oracle_adam8_code_signed(float x, const float* mag7)
+{
+    int k = oracle_nearest(fabsf(x), mag7, 128);
+    return (uint8_t)((x < 0.0f && k > 0) ? (0x80 | k) : k);
+}
+
+/* Code of x in [0, 1] under the unsigned map. */
+uint8_t oracle_adam8_code_unsigned(float x, const float* mag8)
+{
+    return (uint8_t)oracle_nearest(x, mag8, 256);
+}
+
+/* One 8-bit Adam update at Adam time t = step (>= 1) for n coordinates, in
+ * place on master, the codes and the per-block scales, writing fp16(theta')
+ * into params.  For every block of 2048 consecutive elements (the last one may
+ * be shorter), with scales sm, sv of the block:
+ *   m   = (+-mag7[code & 127]) * sm      v = mag8[code] * sv
+ *   m', v', theta' and the fp16 cast as in oracle_adam_apply
+ *   sm' = max |m'| over the block        sv' = max v' over the block
+ *   codes of m' / sm' and v' / sv' (fp32 divisions; 0 when the scale is 0)
+ * Codes 0 with scale 0 stand for m = v = 0 before the first step. */
+int32_t oracle_adam8_apply(const float* g, int64_t n, float* master, uint8_t* m_codes, uint8_t* v_codes,
+                           float* m_scale, float* v_scale, uint16_t* params, double lr, double beta1,
+                           double beta2, double eps, double weight_decay, int64_t step)
+{
+    if (n < 0 || step < 1) return ORACLE_ERR_ARG;
+    if (n > 0 && (g == NULL || master == NULL || m_codes == NULL || v_codes == NULL || m_scale == NULL ||
+                  v_scale == NULL))
+        return ORACLE_ERR_ARG;
+    float mag7[128], mag8[256];
+    oracle_adam8_maps(mag7, mag8);
+
+    double p1 = 1.0, p2 = 1.0;
+    for (int64_t i = 0; i < step; ++i) {
+        p1 = p1 * beta1;
+        p2 = p2 * beta2;
+    }
+    float b1 = (float)beta1, c1 = (float)(1.0 - beta1);
+    float b2 = (float)beta2, c2 = (float)(1.0 - beta2);
+    float bc1 = (float)(1.0 - p1), bc2 = (float)(1.0 - p2);
+    float lr_f = (float)lr, eps_f = (float)eps, wd_f = (float)weight_decay;
+
+    float m_new[ORACLE_ADAM8_BLOCK], v_new[ORACLE_ADAM8_BLOCK];
+    for (int64_t b = 0; b * ORACLE_ADAM8_BLOCK < n; ++b) {
+        int64_t lo = b * ORACLE_ADAM8_BLOCK;
+        int64_t hi = lo + ORACLE_ADAM8_BLOCK < n ? lo + ORACLE_ADAM8_BLOCK : n;
+        float sm = m_scale[b], sv = v_scale[b];
+        float amax_m = 0.0f, amax_v = 0.0f;
+        for (int64_t j = lo; j < hi; ++j) {
+            int cm = m_codes[j];
+            float mag = mag7[cm & 0x7f];
+            float m_old = ((cm & 0x80) ? -mag : mag) * sm;
+            float v_old = mag8[v_codes[j]] * sv;
+            float gj = g[j];
+            float mj = b1 * m_old + c1 * gj;
+            float vj = b2 * v_old + c2 * (gj * gj);
+            float mh = mj / bc1;
+            float vh = vj / bc2;
+            float u = mh / (sqrtf(vh) + eps_f);
+            float th = master[j];
+            float th_new = th - lr_f * (u + wd_f * th);
+            master[j] = th_new;
+            if (params) params[j] = oracle_f32_to_f16(th_new);
+            m_new[j - lo] = mj;
+            v_new[j - lo] = vj;
+            if (fabsf(mj) > amax_m) amax_m = fabsf(mj);
+            if (vj > amax_v) amax_v = vj;
+        }
+        for (int64_t j = lo; j < hi; ++j) {
+            float xm = amax_m > 0.0f ? m_new[j - lo] / amax_m : 0.0f;
+            float xv = amax_v > 0.0f ? v_new[j - lo] / amax_v : 0.0f;
+            m_codes[j] = oracle_adam8_code_signed(xm, mag7);
+            v_codes[j] = oracle_adam8_code_unsigned(xv, mag8);
+        }
+        m_scale[b] = amax_m;
+        v_scale[b] = amax_v;
     }
     return ORACLE_OK;
 }
