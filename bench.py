@@ -53,8 +53,9 @@ def parse_args():
                     help="global gradient-norm clipping at this max norm (two-pass step); 0 = off")
     ap.add_argument("--clip-keep-g", action="store_true",
                     help="with --clip: pass 1 keeps the fp32 reduced gradient for pass 2")
-    ap.add_argument("--optimizer", default="adam", choices=["adam", "sgd"],
-                    help="adam (the pages' mixed-precision Adam) or sgd (SGD with momentum 0.9)")
+    ap.add_argument("--optimizer", default="adam", choices=["adam", "sgd", "adam8"],
+                    help="adam (the pages' mixed-precision Adam), sgd (SGD with momentum 0.9) or adam8 "
+                         "(8-bit Adam: m, v as 8-bit codes with a scale per 2048 elements)")
     ap.add_argument("--qwz", action="store_true",
                     help="keep the int8 qwZ copy of the fp16 shard in each step (1 + 4/256 bytes per element)")
     ap.add_argument("--math", default="fast", choices=["fast", "ieee"],
@@ -89,7 +90,10 @@ def arm_config(args, w, elems: int, bytes_step: int, world: int) -> dict:
     bounded sample of this same workload and says so in its cpu_baseline)."""
     return {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
             "bytes_per_param": round(bytes_step / max(elems, 1), 4), "bytes_per_step": bytes_step,
-            "storage": "fp16 grads and params, fp32 master/m/v (ping-pong)",
+            "storage": {"sgd": "fp16 grads and params, fp32 master/momentum (ping-pong)",
+                        "adam8": "fp16 grads and params, fp32 master, 8-bit m/v codes + fp32 scale per 2048 "
+                                 "(ping-pong)"}.get(getattr(args, "optimizer", "adam"),
+                                                   "fp16 grads and params, fp32 master/m/v (ping-pong)"),
             "math": ("ZS_MATH_FAST: u by corrected hardware reciprocal (within 1 ulp), all else IEEE; "
                      "m/v bit-exact" if args.math == "fast" else "ZS_MATH_IEEE: every fp32 operation IEEE, "
                      "bit-exact"),
@@ -352,8 +356,10 @@ def main():
 
     clip = args.clip > 0
     sgd_hp = binding.sgd(w.lr, 0.9, w.weight_decay)
-    if args.optimizer == "sgd" and (clip or args.qwz):
-        raise SystemExit("--optimizer sgd goes without --clip / --qwz")
+    if args.optimizer != "adam" and (clip or args.qwz):
+        raise SystemExit(f"--optimizer {args.optimizer} goes without --clip / --qwz")
+    if args.optimizer == "adam8":
+        run.enable_adam8()
     if clip:
         run.enable_clipping(args.clip_keep_g)
     if args.qwz:
@@ -362,10 +368,13 @@ def main():
     def one_step(ev=None):
         binding.zero_partition_layout_device(numels_dev, w.n_d, w.align, lay_scalars, lay_toff, lay_soff,
                                              lay_frags, cap, stream=stream)
-        if args.optimizer == "sgd":
+        if args.optimizer in ("sgd", "adam8"):
             if ev is not None:
                 ev[0].record(stream)
-            run.step_sgd(sgd_hp)  # fused kernel(s) and the commit
+            if args.optimizer == "sgd":
+                run.step_sgd(sgd_hp)  # fused kernel(s) and the commit
+            else:
+                run.step_adam8()      # one fused kernel per shard and the commit
             if ev is not None:
                 ev[1].record(stream)
             return
@@ -437,6 +446,8 @@ def main():
     bytes_step = run.clipped_bytes_per_step() if clip else run.bytes_per_step()
     if args.optimizer == "sgd":  # fp32 master + momentum: 2 N_d + 18 bytes per element
         bytes_step = sum((2 * w.n_d + 18) * run.n_valid[r] for r in run.shard_ids)
+    if args.optimizer == "adam8":  # fp32 master + 8-bit m, v: 2 N_d + 14 bytes per element + the scales
+        bytes_step = run.adam8_bytes_per_step()
     if args.qwz:  # int8 codes + one fp32 scale per 256 elements, written by the step
         bytes_step += sum(run.n_valid[r] + 4 * ((run.n_valid[r] + 255) // 256) for r in run.shard_ids)
     hbm_gbs = bytes_step * world * args.steps / (ms_max / 1e3) / 1e9
@@ -480,7 +491,7 @@ def main():
     # end to end through the C ABI with host buffers: pinned H2D of the step's
     # gradient contributions, the step, D2H of the fp16 shard and the control block
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.optimizer == "adam" and not clip and not args.qwz:
         e2e = end_to_end(args, run, stream, dev, world)
 
     line = {
@@ -504,6 +515,11 @@ def main():
     if args.optimizer == "sgd":
         line["optimizer"] = {"kind": "sgd", "momentum": 0.9, "timed": "fused kernel + commit"}
         line["roofline"]["kernel"] = ("sgd_group_kernel" if len(run.views) > 1 else "sgd_step_kernel") + " + commit_kernel"
+    if args.optimizer == "adam8":
+        line["optimizer"] = {"kind": "adam8", "block": binding.ZS_ADAM8_BLOCK,
+                             "state": "fp32 master, uint8 codes of m and v, fp32 scale per block (ping-pong)",
+                             "timed": "fused kernel per shard + commit"}
+        line["roofline"]["kernel"] = "adam8_step_kernel + commit_kernel"
     if args.qwz:
         line["qwz"] = {"block": 256, "extra_bytes_per_param": round(1 + 4 / 256, 4)}
     if clip_info is not None:

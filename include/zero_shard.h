@@ -442,6 +442,70 @@ ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shard
                                          const zs_sgd* hp, zs_ctrl* ctrl_dev, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* 8-bit Adam (the optimizer of state multiplier K = 6, "DeepSpeed ZeRO       */
+/* Stages", sec. 1.2; block-wise quantization after Dettmers et al., "8-bit  */
+/* Optimizers via Block-wise Quantization").                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Elements per quantization block of the 8-bit states. */
+#define ZS_ADAM8_BLOCK 2048
+
+/* One shard of 8-bit Adam state.  As zs_shard, with m and v kept as one byte
+ * per element and one fp32 scale per block of ZS_ADAM8_BLOCK elements (block b
+ * = elements [2048 b, 2048 b + 2048), the last one possibly shorter):
+ *   grads, master, params, n   as in zs_shard;
+ *   m_codes, v_codes           DEVICE uint8[n], two sets (ping-pong with
+ *                              master): bit 7 of an m code is the sign, bits
+ *                              0-6 index the 128 magnitudes of the signed map;
+ *                              a v code indexes the 256 values of the unsigned
+ *                              map (zero_adam8_maps);
+ *   m_scale, v_scale           DEVICE fp32[ceil(n / 2048)], two sets: the
+ *                              block's largest |m| (largest v).
+ * The state value is map[code] * scale; codes and scales all 0 are m = v = 0
+ * (the state before the first step).  With grads and params 16-byte aligned,
+ * master 16-byte and the codes 8-byte aligned a thread moves 8 elements per
+ * access (16 with n_d > 4 and master 32-byte, codes 16-byte aligned); other
+ * naturally aligned buffers take element-wise accesses, same arithmetic. */
+typedef struct zs_adam8_shard {
+    const uint16_t* const* grads;
+    float* master[2];
+    uint8_t* m_codes[2];
+    uint8_t* v_codes[2];
+    float* m_scale[2];
+    float* v_scale[2];
+    uint16_t* params;
+    int64_t n;
+} zs_adam8_shard;
+
+/* The step of zero_shard_step_async with 8-bit states: g, the non-finite
+ * test, the loss scale, t and the ping-pong set as there; then for every
+ * block, reading set cur and writing set cur ^ 1:
+ *   m = +-mag7[m_code & 127] * m_scale,   v = mag8[v_code] * v_scale
+ *   m', v', theta' and params = fp16_rn(theta') as in zero_shard_step
+ *   m_scale' = max |m'| and v_scale' = max v' over the block
+ *   m_code' = the code of the map value nearest to m' / m_scale' (IEEE fp32
+ *   division; 0 when the scale is 0), ties to the smaller magnitude, sign bit
+ *   for a negative quotient with a non-zero magnitude code; v alike.
+ * hp->math applies to u as in zero_shard_step; the codes do not depend on it.
+ * One kernel launch per shard with n > 0, then the device commit (a skipped
+ * step leaves set cur, so codes and scales too, untouched).  Per element
+ * 2 n_d + 14 bytes (+ 16 per block).
+ * Source: "DeepSpeed ZeRO Stages", sec. 1.2 (8-bit Adam, K = 6), with the update of "ZeRO Stage 1
+ * Math", "The per-step mechanics", beats 2-3. */
+ZS_API int32_t zero_shard_step_adam8_async(const zs_adam8_shard* shards, int32_t n_shards, int32_t n_d,
+                                           const zs_adam* hp, zs_ctrl* ctrl_dev, void* stream);
+
+/* The library's two code maps (HOST outputs): mag7[128], the magnitudes of the
+ * signed map for m, and mag8[256], the unsigned map for v.  Code 0 is 0;
+ * code k > 0 has decimal exponent E = (number of leading zero bits of k in a
+ * 7- or 8-bit field) and fraction bits j below its leading one bit (f of
+ * them): value 10^-E (0.1 + 0.9 (j + 1) / 2^f), formed in double, rounded once
+ * to float.  Returns ZS_ERR_ARG for a NULL output.  No CUDA call.
+ * Source: the dynamic map of Dettmers et al., "8-bit Optimizers via Block-wise Quantization", for
+ * the 8-bit Adam of "DeepSpeed ZeRO Stages", sec. 1.2. */
+ZS_API int32_t zero_adam8_maps(float* mag7, float* mag8);
+
+/* ------------------------------------------------------------------------ */
 /* The step on the host CPU cores (ZeRO-Offload, "DeepSpeed ZeRO Stages",     */
 /* sec. 5.1: optimizer state and update on the CPU, with SIMD and threads).  */
 /* ------------------------------------------------------------------------ */

@@ -196,3 +196,71 @@ def test_debug_checks_absent_from_ordinary_build(zs):
         pytest.skip("the debug build is loaded")
     assert zs.zero_debug_checks() == (False, 0)
     assert zs.lib().zero_debug_checks(None) == zs.ZS_ERR_ARG
+
+
+def test_adam8_maps_match_oracle(zs, oracle):
+    """The library builds its code maps on the host from the same definition as
+    the oracle, in code of its own: the tables agree bit for bit."""
+    mag7, mag8 = zs.zero_adam8_maps()
+    o7, o8 = oracle.adam8_maps()
+    assert np.array_equal(mag7.view(np.uint32), o7.view(np.uint32))
+    assert np.array_equal(mag8.view(np.uint32), o8.view(np.uint32))
+    assert zs.lib().zero_adam8_maps(None, None) == zs.ZS_ERR_ARG
+
+
+def _fake_adam8(n=1000, n_d=2):
+    from zero_partitioned_mixed_partition_gb300 import binding
+    table = (ctypes.c_void_p * n_d)(*[0x100000 * (k + 1) for k in range(n_d)])
+    s = binding.Adam8Shard()
+    s.grads = ctypes.cast(table, ctypes.POINTER(ctypes.c_void_p))
+    for i in range(2):
+        s.master[i] = 0x1000000 + 0x100000 * i
+        s.m_codes[i] = 0x2000000 + 0x100000 * i
+        s.v_codes[i] = 0x3000000 + 0x100000 * i
+        s.m_scale[i] = 0x4000000 + 0x100000 * i
+        s.v_scale[i] = 0x5000000 + 0x100000 * i
+    s.params = 0x6000000
+    s.n = n
+    return s, table
+
+
+def test_adam8_argument_checks_refuse_before_cuda(zs):
+    L = zs.lib()
+    hp = zs.adam(1e-3)
+    ctrl = ctypes.c_void_p(0x30000)
+    s, keep = _fake_adam8()
+    arr = (zs.Adam8Shard * 1)(s)
+
+    def call(a=arr, n_shards=1, n_d=2, h=hp, c=ctrl):
+        return L.zero_shard_step_adam8_async(a, n_shards, n_d, ctypes.byref(h), c, None)
+
+    assert call(n_d=0) == zs.ZS_ERR_ARG
+    assert call(n_d=zs.ZS_MAX_ND + 1) == zs.ZS_ERR_ARG
+    assert call(n_shards=0) == zs.ZS_ERR_ARG
+    assert call(c=None) == zs.ZS_ERR_ARG
+    assert call(c=ctypes.c_void_p(0x30004)) == zs.ZS_ERR_ALIGN
+    assert call(h=zs.adam(1e-3, beta2=1.0)) == zs.ZS_ERR_ARG
+    assert call(h=zs.adam(1e-3, math=3)) == zs.ZS_ERR_ARG
+    for field, value, status in (("n", -1, zs.ZS_ERR_ARG), ("params", None, zs.ZS_ERR_ARG),
+                                 ("params", 0x6000001, zs.ZS_ERR_ALIGN)):
+        bad, k = _fake_adam8()
+        setattr(bad, field, value)
+        assert call(a=(zs.Adam8Shard * 1)(bad)) == status, field
+    bad, k = _fake_adam8()
+    bad.v_codes[1] = None
+    assert call(a=(zs.Adam8Shard * 1)(bad)) == zs.ZS_ERR_ARG
+    bad, k = _fake_adam8()
+    bad.m_scale[0] = 0x4000002                  # fp32 scales on a 2-byte boundary
+    assert call(a=(zs.Adam8Shard * 1)(bad)) == zs.ZS_ERR_ALIGN
+    bad, k = _fake_adam8()
+    bad.master[0] = 0x1000002
+    assert call(a=(zs.Adam8Shard * 1)(bad)) == zs.ZS_ERR_ALIGN
+    assert zs.zero_kernel_launches() == 0
+
+
+def test_adam8_struct_layout(zs):
+    """zs_adam8_shard: the contribution table, five pointer pairs, params, n."""
+    assert ctypes.sizeof(zs.Adam8Shard) == 8 + 5 * 16 + 8 + 8
+    assert zs.Adam8Shard.params.offset == 88 and zs.Adam8Shard.n.offset == 96
+    text = open(os.path.join(ROOT, "include", "zero_shard.h")).read()
+    assert re.search(r"#define ZS_ADAM8_BLOCK 2048\b", text) and zs.ZS_ADAM8_BLOCK == 2048

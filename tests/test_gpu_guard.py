@@ -138,3 +138,37 @@ def test_layout_cast_and_qwz_kernels_write_inside(zs, cuda_device):
         back = gd.buf(n, torch.float16, off)
         zs.zero_qwz_dequantize(codes, scales, n, back)
     gd.check("layout / cast / qwz")
+
+
+@pytest.mark.parametrize("n", [1, 7, 2047, 2049, 2048 * 3 + 9])
+@pytest.mark.parametrize("n_d,offset", [(4, 0), (8, 0), (64, 0), (5, 1)])
+def test_adam8_writes_inside_its_buffers(zs, cuda_device, n, n_d, offset):
+    """8-bit Adam: codes, block scales, master and params of two shards (one
+    with an overflow step) between canary bands, every access width."""
+    gd = Guarded(cuda_device)
+
+    def shard(n, seed):
+        grads = [gd.buf(n, torch.float16, offset, synth.random_fp16(n, seed + k, 100.0, device=gd.dev))
+                 for k in range(n_d)]
+        master = (gd.buf(n, torch.float32, offset, synth.random_f32(n, seed, 0.02, device=gd.dev)),
+                  gd.buf(n, torch.float32, offset))
+        nb = (n + 2047) // 2048
+        codes = lambda: gd.buf(n, torch.uint8, offset, torch.zeros(n, dtype=torch.uint8, device=gd.dev))
+        scales = lambda: gd.buf(nb, torch.float32, offset)
+        params = gd.buf(n, torch.float16, offset)
+        return zs.Adam8View(grads, master, (codes(), codes()), (codes(), codes()), (scales(), scales()),
+                            (scales(), scales()), params, n)
+
+    shards = [shard(n, 7), shard(n + 3, 9)]
+    ctrl = gd.buf(zs.CTRL_BYTES // 8 + 1, torch.int64)
+    hp = zs.adam(1e-3, weight_decay=0.01, math=zs.ZS_MATH_FAST)
+    zs.zero_ctrl_init(ctrl, 1024.0)
+    for step in range(1, 4):
+        if step == 2:
+            shards[1].grads[0][n // 2] = float("inf")          # overflow: the commit's restore path
+        zs.zero_shard_step_adam8_async(shards, n_d, hp, ctrl)
+        torch.cuda.synchronize()
+        assert zs.read_ctrl(ctrl)["last_overflow"] == int(step == 2)
+        if step == 2:
+            shards[1].grads[0][n // 2] = 0.0
+    gd.check(f"adam8 n={n} n_d={n_d} offset={offset}")

@@ -26,6 +26,7 @@ ZS_MAX_ND = 1024
 ZS_MAX_SHARDS = 256
 ZS_NOALLOC_MAX_SHARDS = 64
 ZS_QWZ_BLOCK = 256
+ZS_ADAM8_BLOCK = 2048
 ZS_MATH_IEEE, ZS_MATH_FAST = 0, 1
 
 _P = ctypes.c_void_p
@@ -53,6 +54,11 @@ class Adam(ctypes.Structure):
 class Shard(ctypes.Structure):
     _fields_ = [("grads", ctypes.POINTER(_P)), ("master", _P * 2), ("m", _P * 2), ("v", _P * 2),
                 ("params", _P), ("n", _I64), ("qcodes", _P), ("qscales", _P)]
+
+
+class Adam8Shard(ctypes.Structure):
+    _fields_ = [("grads", ctypes.POINTER(_P)), ("master", _P * 2), ("m_codes", _P * 2), ("v_codes", _P * 2),
+                ("m_scale", _P * 2), ("v_scale", _P * 2), ("params", _P), ("n", _I64)]
 
 
 class Sgd(ctypes.Structure):
@@ -93,6 +99,8 @@ _SIGNATURES = {
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
     "zero_shard_step_cpu": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _I32, _P]),
     "zero_shard_step_sgd_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
+    "zero_shard_step_adam8_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
+    "zero_adam8_maps": (_I32, [_P, _P]),
     "zero_qwz_quantize": (_I32, [_P, _I64, _P, _P, _P]),
     "zero_qwz_dequantize": (_I32, [_P, _P, _I64, _P, _P]),
     "zero_status_string": (ctypes.c_char_p, [_I32]),
@@ -288,6 +296,62 @@ def zero_shard_step_sgd_async(shards: Sequence[ShardView], n_d: int, hp: Sgd, ct
     rc = lib().zero_shard_step_sgd_async(arr, len(shards), int(n_d), ctypes.byref(hp),
                                          _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
     _check(rc, "zero_shard_step_sgd_async")
+
+
+# -------------------------------------------------------------- 8-bit Adam ---
+
+class Adam8View:
+    """One shard of 8-bit Adam state and the C struct that describes it.
+
+    grads, params, n as ShardView; master: pair of fp32 CUDA tensors; m_codes,
+    v_codes: pairs of uint8 CUDA tensors (>= n); m_scale, v_scale: pairs of
+    fp32 CUDA tensors (>= ceil(n / ZS_ADAM8_BLOCK))."""
+
+    def __init__(self, grads: Sequence[torch.Tensor], master, m_codes, v_codes, m_scale, v_scale,
+                 params: torch.Tensor, n: int):
+        self.grads = list(grads)
+        self.master, self.m_codes, self.v_codes = tuple(master), tuple(m_codes), tuple(v_codes)
+        self.m_scale, self.v_scale = tuple(m_scale), tuple(v_scale)
+        self.params = params
+        self.n = int(n)
+        blocks = (self.n + ZS_ADAM8_BLOCK - 1) // ZS_ADAM8_BLOCK
+        for pair in (self.m_codes, self.v_codes):
+            if any(t.numel() < self.n for t in pair):
+                raise ValueError("code buffers too small")
+        for pair in (self.m_scale, self.v_scale):
+            if any(t.numel() < blocks for t in pair):
+                raise ValueError("scale buffers too small")
+        self._table = (_P * max(len(self.grads), 1))(
+            *[_dev_ptr(g, torch.float16, "grads") for g in self.grads])
+        self.struct = Adam8Shard()
+        self.struct.grads = ctypes.cast(self._table, ctypes.POINTER(_P))
+        for i in range(2):
+            self.struct.master[i] = _dev_ptr(self.master[i], torch.float32, "master")
+            self.struct.m_codes[i] = _dev_ptr(self.m_codes[i], torch.uint8, "m_codes")
+            self.struct.v_codes[i] = _dev_ptr(self.v_codes[i], torch.uint8, "v_codes")
+            self.struct.m_scale[i] = _dev_ptr(self.m_scale[i], torch.float32, "m_scale")
+            self.struct.v_scale[i] = _dev_ptr(self.v_scale[i], torch.float32, "v_scale")
+        self.struct.params = _dev_ptr(params, torch.float16, "params")
+        self.struct.n = self.n
+
+
+def zero_shard_step_adam8_async(shards: Sequence[Adam8View], n_d: int, hp: Adam, ctrl_dev: torch.Tensor,
+                                stream=None):
+    """Stream-ordered step with 8-bit Adam states."""
+    arr = (Adam8Shard * len(shards))()
+    for i, s in enumerate(shards):
+        arr[i] = s.struct
+    rc = lib().zero_shard_step_adam8_async(arr, len(shards), int(n_d), ctypes.byref(hp),
+                                           _dev_ptr(ctrl_dev, torch.int64, "ctrl_dev"), _stream(stream))
+    _check(rc, "zero_shard_step_adam8_async")
+
+
+def zero_adam8_maps():
+    """The library's code maps: (mag7[128], mag8[256]) float32 numpy arrays."""
+    mag7 = np.empty(128, np.float32)
+    mag8 = np.empty(256, np.float32)
+    _check(lib().zero_adam8_maps(mag7.ctypes.data, mag8.ctypes.data), "zero_adam8_maps")
+    return mag7, mag8
 
 
 def zero_shard_step(shards: Sequence[ShardView], n_d: int, hp: Adam, loss_scale: float, step: int, cur: int,

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(PKG, "libzeroshard.so")
 CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
 CHECKED_LIB_PATH = os.path.join(PKG, "libzeroshard_checked.so")
 
-SOURCES = ["shard_step.cu", "clip.cu", "sgd.cu", "layout.cu", "cpu_step.cpp", "diag.cpp"]
+SOURCES = ["shard_step.cu", "clip.cu", "sgd.cu", "adam8.cu", "layout.cu", "cpu_step.cpp", "diag.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -ffp-contract=off keeps host arithmetic (step coefficients, the CPU step) free
 # of fused multiply-adds, matching the device code's explicit _rn operations;

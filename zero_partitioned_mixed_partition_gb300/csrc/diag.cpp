@@ -67,7 +67,8 @@ ZS_API int32_t zero_debug_checks(uint64_t* first_fault) {
     if (first_fault == nullptr) return ZS_ERR_ARG;
     *first_fault = 0;
 #if ZS_CHECKED
-    const uint64_t faults[] = {zs::take_fault_shard_step(), zs::take_fault_clip(), zs::take_fault_sgd()};
+    const uint64_t faults[] = {zs::take_fault_shard_step(), zs::take_fault_clip(), zs::take_fault_sgd(),
+                               zs::take_fault_adam8()};
     for (uint64_t f : faults) {
         if (f == ~0ull) return zs::fail_with(ZS_ERR_CUDA, "zero_debug_checks: the fault record could not be read");
         if (f != 0 && *first_fault == 0) *first_fault = f;

@@ -59,6 +59,7 @@ int32_t launch_qwz(const float* master, uint16_t* params, int64_t n, int8_t* cod
 uint64_t take_fault_shard_step();
 uint64_t take_fault_clip();
 uint64_t take_fault_sgd();
+uint64_t take_fault_adam8();
 // Enqueues the device-side commit / skip of a step over `shards`.
 int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
                       cudaStream_t stream);

@@ -118,6 +118,22 @@ class WorkloadRunner:
             self.qwz[r] = (codes, scales)
         self.views = views
 
+    def enable_adam8(self):
+        """Give every stepped shard 8-bit Adam state -- uint8 codes of m and v
+        and fp32 scales per 2048-element block, two sets each, all zero (m = v
+        = 0) -- beside the shard's fp32 master and fp16 slice, which it shares."""
+        self.adam8 = {}
+        self.adam8_views = []
+        nb = (self.S + binding.ZS_ADAM8_BLOCK - 1) // binding.ZS_ADAM8_BLOCK
+        for r in self.shard_ids:
+            codes = lambda: torch.zeros(self.S, dtype=torch.uint8, device=self.device)
+            scales = lambda: torch.zeros(nb, dtype=torch.float32, device=self.device)
+            mc, vc, ms, vs = (codes(), codes()), (codes(), codes()), (scales(), scales()), (scales(), scales())
+            master, _, _, params = self.state[r]
+            self.adam8[r] = (mc, vc, ms, vs)
+            self.adam8_views.append(binding.Adam8View(self.grads[r], master, mc, vc, ms, vs, params,
+                                                      self.n_valid[r]))
+
     # ---------------------------------------------------------------- steps --
     def step(self):
         """One whole step over every stepped shard, stream-ordered."""
@@ -126,6 +142,10 @@ class WorkloadRunner:
     def step_sgd(self, hp):
         """One step with SGD with momentum (momentum kept in the m buffers)."""
         binding.zero_shard_step_sgd_async(self.views, self.w.n_d, hp, self.ctrl, stream=self.stream)
+
+    def step_adam8(self):
+        """One step with 8-bit Adam states (enable_adam8 first)."""
+        binding.zero_shard_step_adam8_async(self.adam8_views, self.w.n_d, self.hp, self.ctrl, stream=self.stream)
 
     def reduce_adam(self, i: int = 0):
         binding.zero_shard_reduce_adam_async(self.views[i], self.w.n_d, self.hp, self.ctrl, stream=self.stream)
@@ -173,6 +193,14 @@ class WorkloadRunner:
         master, m, v, params = self.state[r]
         return master[cur], m[cur], v[cur], params
 
+    def current_adam8(self, r: int):
+        """(master, m_codes, v_codes, m_scale, v_scale, params) holding the
+        committed 8-bit Adam state of shard r."""
+        cur = self.ctrl_host()["cur"]
+        master, _, _, params = self.state[r]
+        mc, vc, ms, vs = self.adam8[r]
+        return master[cur], mc[cur], vc[cur], ms[cur], vs[cur], params
+
     # ------------------------------------------------------- checkpointing --
     def save(self) -> dict:
         """Host copy of everything a resumed run needs: the control block's
@@ -205,6 +233,13 @@ class WorkloadRunner:
     def bytes_per_step(self) -> int:
         """Algorithmic HBM bytes of one step: (26 + 2 N_d) per stepped element."""
         return sum((26 + 2 * self.w.n_d) * self.n_valid[r] for r in self.shard_ids)
+
+    def adam8_bytes_per_step(self) -> int:
+        """Algorithmic HBM bytes of one 8-bit Adam step: 2 N_d + 14 per stepped
+        element and 16 per 2048-element block (the scales read and written)."""
+        blk = binding.ZS_ADAM8_BLOCK
+        return sum((2 * self.w.n_d + 14) * self.n_valid[r] + 16 * ((self.n_valid[r] + blk - 1) // blk)
+                   for r in self.shard_ids)
 
     def elements_per_step(self) -> int:
         return sum(self.n_valid[r] for r in self.shard_ids)
