@@ -35,6 +35,9 @@ namespace {
 
 #include "step_common.cuh"
 
+// index-check sites of this file (the shared ones are 1-9)
+constexpr uint32_t kSiteAdam8 = 10, kSiteAdam8Scale = 11;
+
 constexpr int kA8Block = ZS_ADAM8_BLOCK;
 constexpr int kMantBits = 7;                        // buckets per octave: 2^7
 constexpr int kLowOctave = 26;                      // buckets cover [2^-26, 1]; below: bucket 0

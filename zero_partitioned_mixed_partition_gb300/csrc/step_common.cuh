@@ -14,8 +14,7 @@
 // failure wins -- and the caller skips the access; nothing traps or asserts.
 // In the ordinary build ZS_RANGE_OK is the constant true.
 constexpr uint32_t kSiteStep = 1, kSiteQwzFused = 2, kSiteCast = 3, kSiteQwz = 4, kSiteDequant = 5,
-                   kSiteNorm = 6, kSiteClipped = 7, kSiteSgd = 8, kSiteScale = 9,
-                   kSiteAdam8 = 10, kSiteAdam8Scale = 11;
+                   kSiteNorm = 6, kSiteClipped = 7, kSiteSgd = 8, kSiteScale = 9;
 
 #if ZS_CHECKED
 __device__ unsigned long long g_fault;
