@@ -483,9 +483,10 @@ typedef struct zs_adam8_shard {
  *   m = +-mag7[m_code & 127] * m_scale,   v = mag8[v_code] * v_scale
  *   m', v', theta' and params = fp16_rn(theta') as in zero_shard_step
  *   m_scale' = max |m'| and v_scale' = max v' over the block
- *   m_code' = the code of the map value nearest to m' / m_scale' (IEEE fp32
- *   division; 0 when the scale is 0), ties to the smaller magnitude, sign bit
- *   for a negative quotient with a non-zero magnitude code; v alike.
+ *   m_code' = the code of the map value nearest to x = m' * r, r the fp32
+ *   reciprocal of m_scale' (correctly rounded, once per block; x = 0 when the
+ *   scale is 0) clamped to [-1, 1], ties to the smaller magnitude, sign bit for
+ *   a negative x with a non-zero magnitude code; v alike.
  * hp->math applies to u as in zero_shard_step; the codes do not depend on it.
  * One kernel launch per shard with n > 0, then the device commit (a skipped
  * step leaves set cur, so codes and scales too, untouched).  Per element

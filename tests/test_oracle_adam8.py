@@ -9,8 +9,9 @@ What fixes the oracle here, apart from itself:
   - a hand-traced first step (codes worked out by hand from the map);
   - reduction to the pinned fp32 Adam: the first step from a zero state, and
     every step of blocks whose states have one magnitude (x = +-1 is exact);
-  - the decomposition dequantize -> fp32 Adam -> block absmax -> nearest code,
-    checked against the pinned fp32 Adam and a brute-force nearest search;
+  - the decomposition dequantize -> fp32 Adam -> block absmax -> nearest code
+    of m' * (1 / absmax), checked against the pinned fp32 Adam and a
+    brute-force nearest search;
   - block isolation: a spike in one block of 2048 leaves the others alone.
 """
 import numpy as np
@@ -171,8 +172,10 @@ def test_step_is_dequantize_adam_quantize(oracle):
     for b in range(ms.size):
         sl = blk == b
         assert ms[b] == np.abs(m[sl]).max() and vs[b] == v[sl].max()
-    xm = (m / ms[blk]).astype(np.float32).astype(np.float64)
-    xv = (v / vs[blk]).astype(np.float32).astype(np.float64)
+    inv_m = (np.float32(1) / ms).astype(np.float32)                   # one fp32 reciprocal per block
+    inv_v = (np.float32(1) / vs).astype(np.float32)
+    xm = (m * inv_m[blk]).astype(np.float32).astype(np.float64)
+    xv = (v * inv_v[blk]).astype(np.float32).astype(np.float64)
     dm = np.abs(np.abs(xm)[:, None] - mag7[None, :])
     dv = np.abs(xv[:, None] - mag8[None, :])
     km = np.argmin(dm, axis=1)                                         # first minimum: the smaller magnitude
@@ -201,3 +204,30 @@ def test_blocks_are_independent(oracle):
         assert np.array_equal(a_mc[sl], b_mc[sl]) and np.array_equal(a_vc[sl], b_vc[sl])
     assert a_ms[0] == b_ms[0] and a_ms[2] == b_ms[2] and a_ms[1] != b_ms[1]
     assert not np.array_equal(a_mc[B:2 * B], b_mc[B:2 * B])
+
+
+def test_scale_without_finite_reciprocal_clamps(oracle):
+    """A block whose moments decayed below 2^-126: 1 / scale overflows to inf,
+    x = m' * inf is clamped to +-1, so every non-zero m' (v') gets the top
+    code and every zero one code 0; the stored scale stays the block max."""
+    mag7, mag8 = oracle.adam8_maps()
+    rng = np.random.Generator(np.random.PCG64(12))
+    n = B
+    mc = rng.integers(0, 256, n).astype(np.uint8)
+    vc = rng.integers(0, 256, n).astype(np.uint8)
+    mc[:10] = 0                                                       # zero moments stay zero
+    vc[:10] = 0
+    ms = np.array([1e-39], np.float32)                                # subnormal scales
+    vs = np.array([1e-39], np.float32)
+    m_old, v_old = _decode(oracle, mc, vc, ms, vs)
+    g = np.zeros(n, np.float32)
+    master = np.full(n, 0.5, np.float32)
+    oracle.adam8_apply(g, master, mc, vc, ms, vs, None, step=3, **HP)
+    m_new = np.float32(HP["beta1"]) * m_old                           # g = 0: m' = b1 m, v' = b2 v
+    v_new = np.float32(HP["beta2"]) * v_old
+    assert ms[0] == np.abs(m_new).max() and vs[0] == v_new.max()
+    with np.errstate(over="ignore"):
+        assert np.isinf(np.float32(1) / ms[0]) and np.isinf(np.float32(1) / vs[0])
+    want_m = np.where(m_new == 0, 0, np.where(m_new < 0, 0xFF, 0x7F)).astype(np.uint8)
+    want_v = np.where(v_new == 0, 0, 0xFF).astype(np.uint8)
+    assert np.array_equal(mc, want_m) and np.array_equal(vc, want_v)
