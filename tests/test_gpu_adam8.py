@@ -198,3 +198,38 @@ def test_adam8_full_size_sampled_blocks(zs, oracle, cuda_device):
             ref.apply(g, step)
             ref.compare(to_np(master[lo:hi]), to_np(mc[lo:hi]), to_np(vc[lo:hi]), to_np(ms[b:b + 1]),
                         to_np(vs[b:b + 1]), f16_bits(params[lo:hi]), exact=False, what=f"xl block {b} step {step}")
+
+
+@pytest.mark.parametrize("n_d", [4, 16])
+def test_adam8_tiny_scales(zs, oracle, cuda_device, n_d):
+    """Blocks whose moments decayed below 2^-126 (zero gradients, subnormal
+    scales): the new scale has no finite reciprocal, x is clamped, the codes
+    and scales still equal the oracle's, and every table index stays inside."""
+    n = 3 * B + 100
+    w = _workload(n, n_d, grads_fresh_per_step=False)
+    run = WorkloadRunner(w, cuda_device)
+    run.enable_adam8()
+    r = run.shard_ids[0]
+    for g in run.grads[r]:
+        g[: 2 * B].zero_()                                   # blocks 0-1: no gradient; 2-3: ordinary
+    rng = np.random.Generator(np.random.PCG64(13))
+    mc, vc, ms, vs = run.adam8[r]
+    codes_m = rng.integers(0, 256, n).astype(np.uint8)
+    codes_v = rng.integers(0, 256, n).astype(np.uint8)
+    sc_m = np.array([1e-39, 2e-45, 1e-3, 5e-4], np.float32)
+    sc_v = np.array([1e-39, 1e-40, 1e-6, 2e-6], np.float32)
+    mc[0][:n].copy_(torch.from_numpy(codes_m))
+    vc[0][:n].copy_(torch.from_numpy(codes_v))
+    ms[0][:4].copy_(torch.from_numpy(sc_m))
+    vs[0][:4].copy_(torch.from_numpy(sc_v))
+    ref = OracleAdam8(oracle, to_np(run.state[r][0][0][:n]), w)
+    ref.mc[:], ref.vc[:], ref.ms[:], ref.vs[:] = codes_m, codes_v, sc_m, sc_v
+    host = [synth.fp16_bits(g[:n]) for g in run.grads[r]]
+    for step in (1, 2, 3):
+        run.step_adam8()
+        torch.cuda.synchronize()
+        g, bad = ref.reduce(host, w.loss_scale)
+        assert not bad
+        ref.apply(g, step)
+        ref.compare(*_state(run, r, n), exact=True, what=f"tiny scales n_d={n_d} step {step}")
+    assert ref.ms[0] < 2.0 ** -126 and ref.ms[1] == 0.0 or ref.ms[1] < 2.0 ** -126

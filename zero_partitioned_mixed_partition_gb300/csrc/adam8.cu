@@ -28,6 +28,9 @@
 
 #include <cmath>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "zs_internal.h"
 
@@ -36,7 +39,7 @@ namespace {
 #include "step_common.cuh"
 
 // index-check sites of this file (the shared ones are 1-9)
-constexpr uint32_t kSiteAdam8 = 10, kSiteAdam8Scale = 11;
+[[maybe_unused]] constexpr uint32_t kSiteAdam8 = 10, kSiteAdam8Scale = 11;
 
 constexpr int kA8Block = ZS_ADAM8_BLOCK;
 constexpr int kMantBits = 7;                        // buckets per octave: 2^7
@@ -45,12 +48,13 @@ constexpr int kBucketShift = 23 - kMantBits;
 constexpr int kBucketBase = (127 - kLowOctave) << kMantBits;
 constexpr int kBuckets = (kLowOctave << kMantBits) + 1;   // the last one holds 1.0
 
-// The two code maps, their decision thresholds and bucket tables.  Passed to
-// the kernel by value (about 9.7 KB of the 32 KB parameter space) and copied
-// to shared memory by each CTA.
+// What the kernel needs of the two code maps: the signed map's 256 code
+// values (sign bit applied), the unsigned map, their decision thresholds and
+// bucket tables.  Passed to the kernel by value (about 10 KB of the 32 KB
+// parameter space) and copied to shared memory by each CTA.
 struct Maps {
-    float mag7[128];        // signed map (m): magnitudes
-    float mag8[256];        // unsigned map (v)
+    float dec7[256];        // value of each m code: +-mag7[code & 127]
+    float mag8[256];        // value of each v code
     float thr7[128];        // thr7[k]: largest float <= (mag7[k] + mag7[k+1]) / 2; thr7[127] = +inf
     float thr8[256];
     uint8_t bucket7[kBuckets];   // number of thr7 entries below the bucket's first value
@@ -106,6 +110,7 @@ bool build_search(const float* mag, int count, float* thr, uint8_t* bucket) {
 }
 
 struct HostMaps {
+    float mag7[128];        // the signed map's magnitudes
     Maps maps;
     bool ok;
 };
@@ -114,9 +119,10 @@ const HostMaps& host_maps() {
     static const HostMaps built = [] {
         HostMaps h;
         std::memset(&h, 0, sizeof(h));
-        for (int k = 0; k < 128; ++k) h.maps.mag7[k] = map_value(k, 7);
+        for (int k = 0; k < 128; ++k) h.mag7[k] = map_value(k, 7);
+        for (int c = 0; c < 256; ++c) h.maps.dec7[c] = (c & 0x80) ? -h.mag7[c & 0x7f] : h.mag7[c & 0x7f];
         for (int k = 0; k < 256; ++k) h.maps.mag8[k] = map_value(k, 8);
-        h.ok = build_search(h.maps.mag7, 128, h.maps.thr7, h.maps.bucket7) &&
+        h.ok = build_search(h.mag7, 128, h.maps.thr7, h.maps.bucket7) &&
                build_search(h.maps.mag8, 256, h.maps.thr8, h.maps.bucket8);
         return h;
     }();
@@ -125,13 +131,14 @@ const HostMaps& host_maps() {
 
 // ----------------------------------------------------------- device helpers ---
 
-// Index of the map value nearest to a (0 <= a <= 1), ties to the smaller.
-// A NaN a (only from a non-finite step, which the commit drops) gives 0.
+// Index of the map value nearest to min(a, 1) for a >= 0, ties to the
+// smaller; a NaN (0 * inf when a scale below 2^-126 has no finite reciprocal)
+// gives 0, as a nearest search does.  Raising a to 2^-26 moves nothing across
+// a threshold (the lowest is 5e-8); with the clamp to 1 it keeps the bucket
+// index inside the table for every input.
 __device__ __forceinline__ uint32_t nearest_code(float a, const float* thr, const uint8_t* bucket) {
-    a = (a <= 1.0f) ? a : 0.0f;
-    int b = (int)(__float_as_uint(a) >> kBucketShift) - kBucketBase;
-    b = min(max(b, 0), kBuckets - 1);
-    const uint32_t k = bucket[b];
+    a = fminf(fmaxf(a, 0x1p-26f), 1.0f);
+    const uint32_t k = bucket[(__float_as_uint(a) >> kBucketShift) - (uint32_t)kBucketBase];
     return k + (a > thr[k] ? 1u : 0u);
 }
 
@@ -187,68 +194,126 @@ struct A8Args {
     Maps maps;
 };
 
-// One CTA iteration's share of a block: VEC consecutive elements from e, the
-// first `valid` of them real.  Dequantizes, updates, stores master and params,
-// and leaves m', v' (0 past valid) in m, v.  VECLOAD: vector accesses for a
-// full share (the buffers are aligned for them).
-template <int CAP, int VEC, int ND, bool FAST, bool VECLOAD>
-__device__ __forceinline__ uint32_t a8_update(const A8Args<CAP>& p, const Maps& sm, const Coef& c, int cur, int64_t e,
-                                              int valid, float scale_m, float scale_v, float* m, float* v) {
-    float th[VEC], acc[VEC];
-    uint32_t cm[VEC], cv[VEC];
-    const float* th_in = p.master[cur];
-    const bool full = VECLOAD && valid == VEC;
-    if (full) {
-        Mem<VEC>::load_f(th_in + e, th);
-        Codes<VEC>::load(p.mq[cur] + e, cm);
-        Codes<VEC>::load(p.vq[cur] + e, cv);
+// ------------------------------------------------------------------ loads ---
+
+// One thread's share of a block: VEC consecutive elements from e.  The loaders
+// fill th (master), acc (the summed contributions, rank order) and the codes
+// cm, cv.
+
+// all VEC elements exist and the buffers are aligned for vector accesses
+template <int CAP, int VEC, int ND>
+__device__ __forceinline__ void a8_load_global(const A8Args<CAP>& p, int cur, int64_t e, float* th, float* acc,
+                                               uint32_t* cm, uint32_t* cv) {
+    Mem<VEC>::load_f(p.master[cur] + e, th);
+    Codes<VEC>::load(p.mq[cur] + e, cm);
+    Codes<VEC>::load(p.vq[cur] + e, cv);
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
-        sum_contributions<CAP, VEC, ND>(p.grads, p.n_d, e, acc);
-    } else {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            th[j] = 0.0f;
-            acc[j] = 0.0f;
-            cm[j] = cv[j] = 0u;
-            if (j < valid) {
-                th[j] = __ldcs(th_in + e + j);
-                cm[j] = p.mq[cur][e + j];
-                cv[j] = p.vq[cur][e + j];
-                sum_contributions<CAP, 1, ND>(p.grads, p.n_d, e + j, &acc[j]);
-            }
-        }
-    }
-    uint32_t bad = 0;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-        const float mag = sm.mag7[cm[j] & 0x7fu];
-        float mj = __fmul_rn((cm[j] & 0x80u) ? -mag : mag, scale_m);
-        float vj = __fmul_rn(sm.mag8[cv[j]], scale_v);
-        if (j < valid) bad |= nonfinite(acc[j]) ? 1u : 0u;
-        adam_update<FAST>(c, acc[j], th[j], mj, vj);
-        m[j] = j < valid ? mj : 0.0f;
-        v[j] = j < valid ? vj : 0.0f;
-    }
-    float* th_out = p.master[cur ^ 1];
-    if (full) {
-        Mem<VEC>::store_f(th_out + e, th);
-        Mem<VEC>::store_h(p.params + e, th);
-    } else {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            if (j < valid) {
-                Mem<1>::store_f(th_out + e + j, &th[j]);
-                Mem<1>::store_h(p.params + e + j, &th[j]);
-            }
-    }
-    return bad;
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
+    sum_contributions<CAP, VEC, ND>(p.grads, p.n_d, e, acc);
 }
 
-template <int CAP, int VEC, int ND, bool FAST, bool VECLOAD>
-__global__ void __launch_bounds__(a8_threads<VEC>()) adam8_step_kernel(const __grid_constant__ A8Args<CAP> p) {
+// the first `valid` (0..VEC) elements, one at a time; zeros past them (which
+// give m' = v' = 0, so they change no block maximum)
+template <int CAP, int VEC, int ND>
+__device__ __forceinline__ void a8_load_partial(const A8Args<CAP>& p, int cur, int64_t e, int valid, float* th,
+                                                float* acc, uint32_t* cm, uint32_t* cv) {
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        th[j] = 0.0f;
+        acc[j] = 0.0f;
+        cm[j] = cv[j] = 0u;
+        if (j < valid) {
+            th[j] = __ldcs(p.master[cur] + e + j);
+            cm[j] = p.mq[cur][e + j];
+            cv[j] = p.vq[cur][e + j];
+            sum_contributions<CAP, 1, ND>(p.grads, p.n_d, e + j, &acc[j]);
+        }
+    }
+}
+
+// ------------------------------------------------ staged (prefetched) loads ---
+
+// The staged kernel (8 elements per thread, 256 threads) copies each thread's
+// share of the CTA's next block into shared memory with cp.async while it
+// computes the current one.  Each thread reads back only what it copied
+// itself, after waiting for its own copy groups: no barrier, flag or spin is
+// involved.  Stage layout (bytes), for n_d contributions:
+//   [k * 4096 + 16 t]           contribution k, thread t (8 fp16)
+//   [G + 16 t], [G + 4096 + 16 t] master, elements 0-3 and 4-7 (G = n_d * 4096)
+//   [G + 8192 + 8 t]            m codes;  [G + 10240 + 8 t]  v codes
+constexpr int kStageThreads = 256;
+
+__host__ __device__ constexpr int64_t stage_bytes(int n_d) { return (int64_t)n_d * 4096 + 12288; }
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void copy16_async(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void copy8_async(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void copies_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// returns once at most N of this thread's committed copy groups are in flight
+template <int N>
+__device__ __forceinline__ void copies_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int CAP, int ND>
+__device__ __forceinline__ void a8_prefetch(const A8Args<CAP>& p, int cur, int64_t e, unsigned char* st) {
+    const int t = threadIdx.x;
+    const int nd = ND > 0 ? ND : p.n_d;
+#pragma unroll 4
+    for (int k = 0; k < nd; ++k) copy16_async(st + ((int64_t)k * kStageThreads + t) * 16, p.grads[k] + e);
+    unsigned char* s = st + (int64_t)nd * kStageThreads * 16;
+    copy16_async(s + t * 16, p.master[cur] + e);
+    copy16_async(s + 4096 + t * 16, p.master[cur] + e + 4);
+    copy8_async(s + 8192 + t * 8, p.mq[cur] + e);
+    copy8_async(s + 10240 + t * 8, p.vq[cur] + e);
+}
+
+template <int CAP, int ND>
+__device__ __forceinline__ void a8_load_staged(const A8Args<CAP>& p, const unsigned char* st, float* th, float* acc,
+                                               uint32_t* cm, uint32_t* cv) {
+    const int t = threadIdx.x;
+    const int nd = ND > 0 ? ND : p.n_d;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+#pragma unroll 4
+    for (int k = 0; k < nd; ++k) {   // rank order, as sum_contributions
+        float h[8];
+        Mem<16>::load_h8(reinterpret_cast<const uint16_t*>(st + ((int64_t)k * kStageThreads + t) * 16), h);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], h[j]);
+    }
+    const unsigned char* s = st + (int64_t)nd * kStageThreads * 16;
+    const float4 a = *reinterpret_cast<const float4*>(s + t * 16);
+    const float4 b = *reinterpret_cast<const float4*>(s + 4096 + t * 16);
+    th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
+    th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
+    const uint2 wm = *reinterpret_cast<const uint2*>(s + 8192 + t * 8);
+    const uint2 wv = *reinterpret_cast<const uint2*>(s + 10240 + t * 8);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        cm[j] = ((j < 4 ? wm.x : wm.y) >> (8 * (j % 4))) & 0xffu;
+        cv[j] = ((j < 4 ? wv.x : wv.y) >> (8 * (j % 4))) & 0xffu;
+    }
+}
+
+// ------------------------------------------------------------------ kernel ---
+
+// One CTA steps one 2048-element block per loop iteration (persistent grid).
+// VECLOAD: vector accesses for full shares; STAGED: the cp.async pipeline
+// above (VEC = 8 with VECLOAD only).
+// Minimum resident CTAs per SM promised to the compiler: the 16-element
+// kernel (128 threads) is held to 102 registers, five CTAs per SM.
+template <int VEC>
+constexpr int a8_min_blocks() { return VEC == 16 ? 5 : 0; }
+
+template <int CAP, int VEC, int ND, bool FAST, bool VECLOAD, bool STAGED>
+__global__ void __launch_bounds__(a8_threads<VEC>(), a8_min_blocks<VEC>()) adam8_step_kernel(const __grid_constant__ A8Args<CAP> p) {
+    static_assert(!STAGED || (VEC == 8 && VECLOAD), "the staged kernel moves 8 aligned elements per thread");
     constexpr int kThr = a8_threads<VEC>();
     constexpr int kWarps = kThr / 32;
+    extern __shared__ __align__(16) unsigned char stages[];  // STAGED: two stages
     __shared__ Maps sm;
     __shared__ Coef s_coef;
     __shared__ int s_cur;
@@ -273,21 +338,66 @@ __global__ void __launch_bounds__(a8_threads<VEC>()) adam8_step_kernel(const __g
     const int cur = s_cur;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nq = (p.n + kA8Block - 1) / kA8Block;
+    const int64_t stage_sz = STAGED ? stage_bytes(ND > 0 ? ND : p.n_d) : 0;
+    // this thread's share of block qq: all VEC elements exist
+    auto share_full = [&](int64_t qq) {
+        const int64_t e = qq * kA8Block + (int64_t)threadIdx.x * VEC;
+        return qq < nq && e + VEC <= p.n && ZS_RANGE_OK(kSiteAdam8, e, VEC, p.n);
+    };
+    bool staged = false;
+    if constexpr (STAGED) {
+        staged = share_full(blockIdx.x);
+        if (staged) a8_prefetch<CAP, ND>(p, cur, (int64_t)blockIdx.x * kA8Block + threadIdx.x * VEC, stages);
+        copies_commit();
+    }
     uint32_t bad = 0;
     int par = 0;
     for (int64_t q = blockIdx.x; q < nq; q += gridDim.x, par ^= 1) {
         const int64_t e = q * kA8Block + (int64_t)threadIdx.x * VEC;
         const int64_t rem = p.n - e;
         const int valid = rem >= VEC ? VEC : (rem > 0 ? (int)rem : 0);
-        if (!ZS_RANGE_OK(kSiteAdam8Scale, q, 1, nq)) continue;   // (uniform over the CTA)
-        const bool in_range = valid == 0 || ZS_RANGE_OK(kSiteAdam8, e, valid, p.n);
-        const float scale_m = p.ms[cur][q], scale_v = p.vs[cur][q];
+        const bool scale_ok = ZS_RANGE_OK(kSiteAdam8Scale, q, 1, nq);
+        const float scale_m = scale_ok ? p.ms[cur][q] : 0.0f, scale_v = scale_ok ? p.vs[cur][q] : 0.0f;
+        float th[VEC], acc[VEC];
+        uint32_t cm[VEC], cv[VEC];
+        bool full;  // this share moves by vector accesses
+        if constexpr (STAGED) {
+            const int64_t qn = q + gridDim.x;
+            const bool next = share_full(qn);
+            if (next) a8_prefetch<CAP, ND>(p, cur, qn * kA8Block + (int64_t)threadIdx.x * VEC, stages + (par ^ 1) * stage_sz);
+            copies_commit();
+            copies_wait<1>();  // this block's copies have landed
+            full = staged;
+            if (full) a8_load_staged<CAP, ND>(p, stages + par * stage_sz, th, acc, cm, cv);
+            staged = next;
+        } else {
+            full = VECLOAD && valid == VEC && ZS_RANGE_OK(kSiteAdam8, e, VEC, p.n);
+            if (full) a8_load_global<CAP, VEC, ND>(p, cur, e, th, acc, cm, cv);
+        }
+        const int live = full ? VEC : (ZS_RANGE_OK(kSiteAdam8, e, valid, p.n) ? valid : 0);
+        if (!full) a8_load_partial<CAP, VEC, ND>(p, cur, e, live, th, acc, cm, cv);
+        // dequantize, update, cast
         float m[VEC], v[VEC];
-        if (in_range) {
-            bad |= a8_update<CAP, VEC, ND, FAST, VECLOAD>(p, sm, c, cur, e, valid, scale_m, scale_v, m, v);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            float mj = __fmul_rn(sm.dec7[cm[j]], scale_m);
+            float vj = __fmul_rn(sm.mag8[cv[j]], scale_v);
+            bad |= nonfinite(acc[j]) ? 1u : 0u;
+            adam_update<FAST>(c, acc[j], th[j], mj, vj);
+            m[j] = mj;
+            v[j] = vj;
+        }
+        float* th_out = p.master[cur ^ 1];
+        if (full) {
+            Mem<VEC>::store_f(th_out + e, th);
+            Mem<VEC>::store_h(p.params + e, th);
         } else {
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) m[j] = v[j] = 0.0f;
+            for (int j = 0; j < VEC; ++j)
+                if (j < live) {
+                    Mem<1>::store_f(th_out + e + j, &th[j]);
+                    Mem<1>::store_h(p.params + e + j, &th[j]);
+                }
         }
         // the block's largest |m'| and v'
         float am = 0.0f, av = 0.0f;
@@ -305,7 +415,7 @@ __global__ void __launch_bounds__(a8_threads<VEC>()) adam8_step_kernel(const __g
             s_red[par][0][warp] = am;
             s_red[par][1][warp] = av;
         }
-        __syncthreads();   // one barrier per block: the parity slot is not rewritten before every warp read it
+        __syncthreads();  // one barrier per block: a parity slot is not rewritten before every warp read it
         am = s_red[par][0][0];
         av = s_red[par][1][0];
 #pragma unroll
@@ -313,34 +423,34 @@ __global__ void __launch_bounds__(a8_threads<VEC>()) adam8_step_kernel(const __g
             am = fmaxf(am, s_red[par][0][w]);
             av = fmaxf(av, s_red[par][1][w]);
         }
-        // codes of m' / am and v' / av
-        uint32_t cm[VEC], cv[VEC];
+        // codes of m' * (1 / am) and v' * (1 / av), one rounded reciprocal per block
+        const float rm = am > 0.0f ? __frcp_rn(am) : 0.0f;
+        const float rv = av > 0.0f ? __frcp_rn(av) : 0.0f;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            const float xm = am > 0.0f ? __fdiv_rn(m[j], am) : 0.0f;
-            const float xv = av > 0.0f ? __fdiv_rn(v[j], av) : 0.0f;
+            const float xm = __fmul_rn(m[j], rm);
+            const float xv = __fmul_rn(v[j], rv);
             const uint32_t k = nearest_code(fabsf(xm), sm.thr7, sm.bucket7);
             cm[j] = (xm < 0.0f && k > 0u) ? (k | 0x80u) : k;
             cv[j] = nearest_code(fabsf(xv), sm.thr8, sm.bucket8);
         }
-        if (in_range && valid > 0) {
-            if (VECLOAD && valid == VEC) {
-                Codes<VEC>::store(p.mq[cur ^ 1] + e, cm);
-                Codes<VEC>::store(p.vq[cur ^ 1] + e, cv);
-            } else {
+        if (full) {
+            Codes<VEC>::store(p.mq[cur ^ 1] + e, cm);
+            Codes<VEC>::store(p.vq[cur ^ 1] + e, cv);
+        } else {
 #pragma unroll
-                for (int j = 0; j < VEC; ++j)
-                    if (j < valid) {
-                        p.mq[cur ^ 1][e + j] = (uint8_t)cm[j];
-                        p.vq[cur ^ 1][e + j] = (uint8_t)cv[j];
-                    }
-            }
+            for (int j = 0; j < VEC; ++j)
+                if (j < live) {
+                    p.mq[cur ^ 1][e + j] = (uint8_t)cm[j];
+                    p.vq[cur ^ 1][e + j] = (uint8_t)cv[j];
+                }
         }
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0 && scale_ok) {
             p.ms[cur ^ 1][q] = am;
             p.vs[cur ^ 1][q] = av;
         }
     }
+    if constexpr (STAGED) copies_wait<0>();  // (the last group is empty) nothing in flight at exit
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
 }
 
@@ -376,13 +486,45 @@ int32_t check_a8_shard(const zs_adam8_shard& s, int32_t n_d, int* width) {
     return ZS_OK;
 }
 
-template <int CAP, int VEC, int ND, bool FAST, bool VECLOAD>
+// Persistent grid of a kernel with `smem` bytes of dynamic shared memory:
+// every SM filled at the kernel's occupancy, at most one CTA per block.
+int a8_blocks(const void* kernel, int threads, size_t smem, int64_t nq) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, size_t>, int> per_sm;
+    int bps = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = per_sm.find({kernel, smem});
+        if (it != per_sm.end()) bps = it->second;
+    }
+    if (bps == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, threads, smem) != cudaSuccess || bps < 1)
+            bps = 1;
+        std::lock_guard<std::mutex> lock(mu);
+        per_sm[{kernel, smem}] = bps;
+    }
+    const int64_t full = (int64_t)bps * zs::device_sm_count();
+    return (int)(nq < full ? (nq < 1 ? 1 : nq) : full);
+}
+
+// Contributions up to which the staged kernel is used (its two stages take
+// 2 (4096 N_d + 12288) bytes of shared memory per CTA).
+constexpr int kStagedMaxNd = 8;
+
+template <int CAP, int VEC, int ND, bool FAST, bool VECLOAD, bool STAGED>
 int32_t launch_a8(const A8Args<CAP>& a, cudaStream_t stream) {
-    const void* k = (const void*)adam8_step_kernel<CAP, VEC, ND, FAST, VECLOAD>;
+    const void* k = (const void*)adam8_step_kernel<CAP, VEC, ND, FAST, VECLOAD, STAGED>;
     constexpr int threads = a8_threads<VEC>();
     const int64_t nq = (a.n + kA8Block - 1) / kA8Block;
-    const int blocks = zs::persistent_blocks(k, threads, nq * threads);
-    adam8_step_kernel<CAP, VEC, ND, FAST, VECLOAD><<<blocks, threads, 0, stream>>>(a);
+    size_t smem = 0;
+    if constexpr (STAGED) {
+        static const cudaError_t attr = cudaFuncSetAttribute(
+            k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(2 * stage_bytes(ND > 0 ? ND : kStagedMaxNd)));
+        if (attr != cudaSuccess) return zs::cuda_fail(attr, "adam8_step_kernel: shared memory attribute");
+        smem = (size_t)(2 * stage_bytes(ND > 0 ? ND : a.n_d));
+    }
+    const int blocks = a8_blocks(k, threads, smem, nq);
+    adam8_step_kernel<CAP, VEC, ND, FAST, VECLOAD, STAGED><<<blocks, threads, smem, stream>>>(a);
     return zs::check_launch("adam8_step_kernel");
 }
 
@@ -406,13 +548,22 @@ int32_t launch_a8_cap(const zs_adam8_shard& s, int32_t n_d, int width, const zs_
     a.flag = &ctrl->overflow;
     a.maps = host_maps().maps;
     const bool fast = hp.math == ZS_MATH_FAST;
+    // up to 8 contributions: the staged 8-element kernel; above, the 16-element
+    // one (whose many contribution loads per thread hide the latency)
+    if constexpr (ND == 0 && CAP <= 16) {
+        if (width >= 1 && n_d <= kStagedMaxNd)
+            return fast ? launch_a8<CAP, 8, ND, true, true, true>(a, stream)
+                        : launch_a8<CAP, 8, ND, false, true, true>(a, stream);
+    }
     if constexpr (ND == 0 || ND > 4) {
         if (width == 2 && n_d > 4)
-            return fast ? launch_a8<CAP, 16, ND, true, true>(a, stream) : launch_a8<CAP, 16, ND, false, true>(a, stream);
+            return fast ? launch_a8<CAP, 16, ND, true, true, false>(a, stream)
+                        : launch_a8<CAP, 16, ND, false, true, false>(a, stream);
     }
     if (width >= 1)
-        return fast ? launch_a8<CAP, 8, ND, true, true>(a, stream) : launch_a8<CAP, 8, ND, false, true>(a, stream);
-    return launch_a8<CAP, 8, ND, false, false>(a, stream);
+        return fast ? launch_a8<CAP, 8, ND, true, true, false>(a, stream)
+                    : launch_a8<CAP, 8, ND, false, true, false>(a, stream);
+    return launch_a8<CAP, 8, ND, false, false, false>(a, stream);
 }
 
 int32_t launch_a8_shard(const zs_adam8_shard& s, int32_t n_d, int width, const zs_adam& hp, zs_ctrl* ctrl,
@@ -441,7 +592,7 @@ ZS_API int32_t zero_adam8_maps(float* mag7, float* mag8) {
     if (mag7 == nullptr || mag8 == nullptr) return ZS_ERR_ARG;
     const HostMaps& h = host_maps();
     if (!h.ok) return zs::fail_with(ZS_ERR_ARG, "zero_adam8_maps: a bucket of the code search holds two thresholds");
-    std::memcpy(mag7, h.maps.mag7, sizeof(h.maps.mag7));
+    std::memcpy(mag7, h.mag7, sizeof(h.mag7));
     std::memcpy(mag8, h.maps.mag8, sizeof(h.maps.mag8));
     return ZS_OK;
 }
