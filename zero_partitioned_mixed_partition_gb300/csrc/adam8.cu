@@ -144,18 +144,42 @@ __device__ __forceinline__ uint32_t nearest_code(float a, const float* thr, cons
 
 // VEC one-byte codes per thread: one 8- or 16-byte access.
 template <int VEC> struct Codes;
+// x / d rounded once to nearest, for d = 1 - beta^t (0 < d <= 1, a per-step
+// constant) with y = RN(1 / d) formed once: q = x y, then two corrections
+// q <- q + (x - d q) y whose residuals the fused multiply-add forms exactly.
+// After the first, q is within one ulp of x / d (a faithful quotient); then
+// its residual is exact and, y being the correctly rounded reciprocal, the
+// second correction yields the correctly rounded quotient (Markstein's
+// theorem; P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", 1990; also Cornea, Harrison and Tang, "Scientific
+// Computing on Itanium-based Systems", 2002).  Valid for x = 0 and for
+// |x| >= 2^-100, where no quotient, product or residual leaves the normal
+// range; the caller sends smaller values to the IEEE division.
+__device__ __forceinline__ float div_by_constant(float x, float d, float y) {
+    float q = __fmul_rn(x, y);
+    q = __fmaf_rn(__fmaf_rn(-q, d, x), y, q);
+    return __fmaf_rn(__fmaf_rn(-q, d, x), y, q);
+}
+
+// Byte j of w, zero-extended; and four codes (each < 256) packed into a word
+// (byte permutes: one instruction per byte out, three per word in).
+__device__ __forceinline__ uint32_t byte_of(uint32_t w, int j) { return __byte_perm(w, 0u, 0x4440u + (uint32_t)j); }
+__device__ __forceinline__ uint32_t pack4(const uint32_t* c) {
+    return __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u), 0x5410u);
+}
 template <> struct Codes<8> {
-    static __device__ __forceinline__ void load(const uint8_t* p, uint32_t* c) {
-        const uint2 r = __ldcs(reinterpret_cast<const uint2*>(p));
-        const uint32_t w[2] = {r.x, r.y};
+    static __device__ __forceinline__ void unpack(uint2 r, uint32_t* c) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) c[j] = (w[j / 4] >> (8 * (j % 4))) & 0xffu;
+        for (int j = 0; j < 4; ++j) {
+            c[j] = byte_of(r.x, j);
+            c[4 + j] = byte_of(r.y, j);
+        }
+    }
+    static __device__ __forceinline__ void load(const uint8_t* p, uint32_t* c) {
+        unpack(__ldcs(reinterpret_cast<const uint2*>(p)), c);
     }
     static __device__ __forceinline__ void store(uint8_t* p, const uint32_t* c) {
-        uint32_t w[2] = {0u, 0u};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[j / 4] |= c[j] << (8 * (j % 4));
-        __stcs(reinterpret_cast<uint2*>(p), make_uint2(w[0], w[1]));
+        __stcs(reinterpret_cast<uint2*>(p), make_uint2(pack4(c), pack4(c + 4)));
     }
 };
 template <> struct Codes<16> {
@@ -163,13 +187,10 @@ template <> struct Codes<16> {
         const uint4 r = *reinterpret_cast<const uint4*>(p);
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) c[j] = (w[j / 4] >> (8 * (j % 4))) & 0xffu;
+        for (int j = 0; j < 16; ++j) c[j] = byte_of(w[j / 4], j % 4);
     }
     static __device__ __forceinline__ void store(uint8_t* p, const uint32_t* c) {
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j / 4] |= c[j] << (8 * (j % 4));
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(p) = make_uint4(pack4(c), pack4(c + 4), pack4(c + 8), pack4(c + 12));
     }
 };
 
@@ -289,13 +310,8 @@ __device__ __forceinline__ void a8_load_staged(const A8Args<CAP>& p, const unsig
     const float4 b = *reinterpret_cast<const float4*>(s + 4096 + t * 16);
     th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
     th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
-    const uint2 wm = *reinterpret_cast<const uint2*>(s + 8192 + t * 8);
-    const uint2 wv = *reinterpret_cast<const uint2*>(s + 10240 + t * 8);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        cm[j] = ((j < 4 ? wm.x : wm.y) >> (8 * (j % 4))) & 0xffu;
-        cv[j] = ((j < 4 ? wv.x : wv.y) >> (8 * (j % 4))) & 0xffu;
-    }
+    Codes<8>::unpack(*reinterpret_cast<const uint2*>(s + 8192 + t * 8), cm);
+    Codes<8>::unpack(*reinterpret_cast<const uint2*>(s + 10240 + t * 8), cv);
 }
 
 // ------------------------------------------------------------------ kernel ---
@@ -303,10 +319,15 @@ __device__ __forceinline__ void a8_load_staged(const A8Args<CAP>& p, const unsig
 // One CTA steps one 2048-element block per loop iteration (persistent grid).
 // VECLOAD: vector accesses for full shares; STAGED: the cp.async pipeline
 // above (VEC = 8 with VECLOAD only).
-// Minimum resident CTAs per SM promised to the compiler: the 16-element
-// kernel (128 threads) is held to 102 registers, five CTAs per SM.
+// Minimum resident CTAs per SM promised to the compiler.  Four for the
+// 16-element kernel (128 threads, at most 128 registers): measured on the
+// 7.5B-parameter N_d = 64 shard, 47.6 Gparams/s (6.76 TB/s) against 28.9 with
+// no promise (the compiler then took 124 registers and ran slower) and 32.3
+// with five CTAs (102 registers, spills).  Three for the 8-element kernels
+// (256 threads, at most 85 registers), the most the staged kernel's shared
+// memory allows anyway.
 template <int VEC>
-constexpr int a8_min_blocks() { return VEC == 16 ? 5 : 0; }
+constexpr int a8_min_blocks() { return VEC == 16 ? 4 : 3; }
 
 template <int CAP, int VEC, int ND, bool FAST, bool VECLOAD, bool STAGED>
 __global__ void __launch_bounds__(a8_threads<VEC>(), a8_min_blocks<VEC>()) adam8_step_kernel(const __grid_constant__ A8Args<CAP> p) {
@@ -335,6 +356,7 @@ __global__ void __launch_bounds__(a8_threads<VEC>(), a8_min_blocks<VEC>()) adam8
     }
     __syncthreads();
     const Coef c = s_coef;
+    const float rcp_bc1 = __frcp_rn(c.bc1), rcp_bc2 = __frcp_rn(c.bc2);
     const int cur = s_cur;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nq = (p.n + kA8Block - 1) / kA8Block;
@@ -377,15 +399,39 @@ __global__ void __launch_bounds__(a8_threads<VEC>(), a8_min_blocks<VEC>()) adam8
         const int live = full ? VEC : (ZS_RANGE_OK(kSiteAdam8, e, valid, p.n) ? valid : 0);
         if (!full) a8_load_partial<CAP, VEC, ND>(p, cur, e, live, th, acc, cm, cv);
         // dequantize, update, cast
+        // the Adam update of the fp32 step, operation for operation, in two
+        // phases so that the bias corrections can use the exact division below
         float m[VEC], v[VEC];
+        float low = 1.0f;  // smallest |m'|, v' of this thread's share
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            float mj = __fmul_rn(sm.dec7[cm[j]], scale_m);
-            float vj = __fmul_rn(sm.mag8[cv[j]], scale_v);
+            const float g = __fmul_rn(acc[j], c.inv);
             bad |= nonfinite(acc[j]) ? 1u : 0u;
-            adam_update<FAST>(c, acc[j], th[j], mj, vj);
-            m[j] = mj;
-            v[j] = vj;
+            m[j] = __fadd_rn(__fmul_rn(c.b1, __fmul_rn(sm.dec7[cm[j]], scale_m)), __fmul_rn(c.c1, g));
+            v[j] = __fadd_rn(__fmul_rn(c.b2, __fmul_rn(sm.mag8[cv[j]], scale_v)), __fmul_rn(c.c2, __fmul_rn(g, g)));
+            low = fminf(low, fminf(fabsf(m[j]), v[j]));
+        }
+        // m' / (1 - beta1^t), v' / (1 - beta2^t): exact by two corrections,
+        // unless a warp holds a value below 2^-100 (or 0): then IEEE divisions
+        float mh[VEC], vh[VEC];
+        if (__any_sync(0xffffffffu, !(low >= 0x1p-100f))) {  // (warp-uniform)
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                mh[j] = __fdiv_rn(m[j], c.bc1);
+                vh[j] = __fdiv_rn(v[j], c.bc2);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                mh[j] = div_by_constant(m[j], c.bc1, rcp_bc1);
+                vh[j] = div_by_constant(v[j], c.bc2, rcp_bc2);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const float den = __fadd_rn(__fsqrt_rn(vh[j]), c.eps);
+            const float u = FAST ? div_corrected(mh[j], den) : __fdiv_rn(mh[j], den);
+            th[j] = __fsub_rn(th[j], __fmul_rn(c.lr, __fadd_rn(u, __fmul_rn(c.wd, th[j]))));
         }
         float* th_out = p.master[cur ^ 1];
         if (full) {
@@ -548,15 +594,17 @@ int32_t launch_a8_cap(const zs_adam8_shard& s, int32_t n_d, int width, const zs_
     a.flag = &ctrl->overflow;
     a.maps = host_maps().maps;
     const bool fast = hp.math == ZS_MATH_FAST;
-    // up to 8 contributions: the staged 8-element kernel; above, the 16-element
-    // one (whose many contribution loads per thread hide the latency)
+    // Up to 8 contributions: the staged 8-element kernel.  9-16: the direct
+    // 8-element kernel, whose contribution loads already keep enough bytes in
+    // flight (ragged workload, N_d = 16: 128.0 Gparams/s against 124.9 for the
+    // 16-element kernel).  Above 16: the 16-element kernel.
     if constexpr (ND == 0 && CAP <= 16) {
         if (width >= 1 && n_d <= kStagedMaxNd)
             return fast ? launch_a8<CAP, 8, ND, true, true, true>(a, stream)
                         : launch_a8<CAP, 8, ND, false, true, true>(a, stream);
     }
-    if constexpr (ND == 0 || ND > 4) {
-        if (width == 2 && n_d > 4)
+    if constexpr (ND == 0 || ND > 16) {
+        if (width == 2 && n_d > 16)
             return fast ? launch_a8<CAP, 16, ND, true, true, false>(a, stream)
                         : launch_a8<CAP, 16, ND, false, true, false>(a, stream);
     }
