@@ -129,24 +129,28 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = [os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc", f)
-                  for f in ("shard_step.cu", "step_common.cuh")]
+# Per step kind: the committed DRAM-traffic record of its dominant kernel and
+# the sources that kernel is compiled from (the record holds their digest).
+TRAFFIC_RECORDS = {
+    "adam": ("shard_step_kernel_traffic.txt", ("shard_step.cu", "step_common.cuh")),
+    "adam8": ("adam8_step_kernel_traffic.txt", ("adam8.cu", "step_common.cuh")),
+}
 
 
-def kernel_source_digest() -> str:
-    """sha256 prefix over the sources the fused step kernel is compiled from."""
+def kernel_source_digest(kind: str = "adam") -> str:
+    """sha256 prefix over the sources the step kind's kernel is compiled from."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        h.update(open(f, "rb").read())
+    for f in TRAFFIC_RECORDS[kind][1]:
+        h.update(open(os.path.join(ROOT, "zero_partitioned_mixed_partition_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(kind: str = "adam"):
     """DRAM bytes per stepped parameter from the committed ncu summary, valid
     only while the kernel sources are unchanged (else None)."""
-    path = os.path.join(ROOT, "profiles", "shard_step_kernel_traffic.txt")
+    path = os.path.join(ROOT, "profiles", TRAFFIC_RECORDS[kind][0])
     try:
-        digest = kernel_source_digest()
+        digest = kernel_source_digest(kind)
         vals = {}
         for line in open(path):
             if ":" in line and not line.startswith("#"):
@@ -470,10 +474,11 @@ def main():
     # roofline of the dominant kernel: algorithmic bytes per launch / mean launch time
     mean_kern_ms = statistics.mean(kern_ms)
     achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
-    traffic_per_param = recorded_traffic()
     traffic = None
-    if traffic_per_param and w.n_d in traffic_per_param and not clip and not args.qwz and args.optimizer == "adam":
-        traffic = round(traffic_per_param[w.n_d] * elems)
+    if args.optimizer in TRAFFIC_RECORDS and not clip and not args.qwz:
+        traffic_per_param = recorded_traffic(args.optimizer)
+        if traffic_per_param and w.n_d in traffic_per_param:
+            traffic = round(traffic_per_param[w.n_d] * elems)
     clip_info = None
     if clip:
         # per pass: algorithmic bytes / mean launch time (pass 1 reads the
