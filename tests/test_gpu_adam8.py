@@ -233,3 +233,92 @@ def test_adam8_tiny_scales(zs, oracle, cuda_device, n_d):
         ref.apply(g, step)
         ref.compare(*_state(run, r, n), exact=True, what=f"tiny scales n_d={n_d} step {step}")
     assert ref.ms[0] < 2.0 ** -126 and ref.ms[1] == 0.0 or ref.ms[1] < 2.0 ** -126
+
+
+def _adam8_views(zs, dev, w, sizes, misaligned):
+    """Fresh buffers per shard; shard i one element off its alignment (the
+    element-wise kernel) when listed.  Returns the views and host contribs."""
+    views, host = [], []
+    for i, n in enumerate(sizes):
+        off = 1 if i in misaligned else 0
+        nb = (n + B - 1) // B
+        grads = []
+        for k in range(w.n_d):
+            t = torch.zeros(n + 16, dtype=torch.float16, device=dev)[off:off + n]
+            t.copy_(synth.grad_contribution(w, n, k, 1, shard=i, device=dev))
+            grads.append(t)
+        f32 = lambda: torch.zeros(n + 16, dtype=torch.float32, device=dev)[off:off + n]
+        u8 = lambda: torch.zeros(n + 32, dtype=torch.uint8, device=dev)[off:off + n]
+        sc = lambda: torch.zeros(nb + 4, dtype=torch.float32, device=dev)[off:off + nb]
+        master = (f32(), f32())
+        master[0].copy_(synth.master_init(w, n, shard=i, device=dev))
+        params = torch.zeros(n + 16, dtype=torch.float16, device=dev)[off:off + n]
+        if n:
+            zs.zero_params_from_master(master[0], params, n)
+        views.append(zs.Adam8View(grads, master, (u8(), u8()), (u8(), u8()), (sc(), sc()), (sc(), sc()), params, n))
+        host.append([synth.fp16_bits(g) for g in grads])
+    return views, host
+
+
+@pytest.mark.parametrize("n_d,sizes,misaligned", [
+    (4, [int(x) for x in np.random.Generator(np.random.PCG64(21)).integers(0, 9000, 37)], ()),   # groups of 16
+    (8, [3 * B + 5, 0, B, 2 * B + 1, 777, 5000, 6, 3000, 4 * B], (3,)),                          # cut by a misaligned shard
+    (16, [B + 3, 17, 0, 250, 4099, 2 * B], ()),
+    (64, [B - 1, 300, 2 * B + 9], (1,)),
+])
+def test_adam8_grouped_launches(zs, oracle, cuda_device, n_d, sizes, misaligned):
+    """Consecutive shards of one access width share a launch (up to 16) that
+    walks their blocks back to back; empty shards join any group; the result
+    equals the oracle bit for bit, with an overflow in one shard on step 2."""
+    w = _workload(1, n_d, grads_fresh_per_step=False, seed=len(sizes) + n_d)
+    views, host = _adam8_views(zs, cuda_device, w, sizes, misaligned)
+    refs = [OracleAdam8(oracle, to_np(v.master[0]), w) for v in views]
+    ctrl = zs.new_ctrl(cuda_device)
+    zs.zero_ctrl_init(ctrl, w.loss_scale)
+    hp = zs.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    victim = max(range(len(sizes)), key=lambda i: sizes[i])
+    ls, applied = w.loss_scale, 0
+    for step in range(1, 4):
+        inject = step == 2
+        j = sizes[victim] // 2
+        if inject:
+            keep = views[victim].grads[0][j].clone()
+            views[victim].grads[0][j] = float("inf")
+        launches = zs.zero_kernel_launches()
+        zs.zero_shard_step_adam8_async(views, n_d, hp, ctrl)
+        torch.cuda.synchronize()
+        reduced, ovf = [], 0
+        for ref, v in zip(refs, views):
+            g, bad = ref.reduce([synth.fp16_bits(t) for t in v.grads], ls)
+            reduced.append(g)
+            ovf |= bad
+        if not ovf:
+            for ref, g in zip(refs, reduced):
+                ref.apply(g, applied + 1)
+        ls, applied = oracle.commit(ovf, ls, applied)
+        c = zs.read_ctrl(ctrl)
+        assert ovf == int(inject) and c["last_overflow"] == ovf and c["step"] == applied
+        if inject:
+            views[victim].grads[0][j] = keep
+        cur = c["cur"]
+        for i, (ref, v) in enumerate(zip(refs, views)):
+            if not sizes[i]:
+                continue
+            nb = (sizes[i] + B - 1) // B
+            ref.compare(to_np(v.master[cur]), to_np(v.m_codes[cur]), to_np(v.v_codes[cur]), to_np(v.m_scale[cur][:nb]),
+                        to_np(v.v_scale[cur][:nb]), f16_bits(v.params), exact=True,
+                        what=f"n_d={n_d} shard {i} step {step}")
+    # one launch per group: runs of one width, at most 16 shards each, plus the commit
+    live = [i for i, n in enumerate(sizes) if n]
+    groups, i = 0, 0
+    widths = [0 if k in misaligned else 1 for k in range(len(sizes))]
+    while i < len(sizes):
+        if not sizes[i]:
+            i += 1
+            continue
+        k = i + 1
+        while k < len(sizes) and k - i < 16 and (not sizes[k] or widths[k] == widths[i]):
+            k += 1
+        groups += 1
+        i = k
+    assert live and zs.zero_kernel_launches() - launches == groups + 1
