@@ -88,7 +88,7 @@ def workload(args):
 def arm_config(args, w, elems: int, bytes_step: int, world: int) -> dict:
     """The workload description both arms print (the reference arm times a
     bounded sample of this same workload and says so in its cpu_baseline)."""
-    return {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
+    return {"workload": workload_label(w, elems, getattr(args, "optimizer", "adam")), "n_d": w.n_d, "shard_params": elems,
             "bytes_per_param": round(bytes_step / max(elems, 1), 4), "bytes_per_step": bytes_step,
             "storage": {"sgd": "fp16 grads and params, fp32 master/momentum (ping-pong)",
                         "adam8": "fp16 grads and params, fp32 master, 8-bit m/v codes + fp32 scale per 2048 "
@@ -114,9 +114,10 @@ def shard_elements(w) -> int:
     return valid[w.rank] if w.rank is not None else sum(valid)
 
 
-def workload_label(w, n_valid):
+def workload_label(w, n_valid, optimizer: str = "adam"):
+    state = {"sgd": "fp32 master/momentum", "adam8": "fp32 master + 8-bit m/v"}.get(optimizer, "fp32 master/m/v")
     return (f"{w.name}: Psi={w.psi:,} ({len(w.numels)} tensors), N_d={w.n_d}, "
-            f"rank {w.rank} shard of {n_valid:,} params, fp16 grads x{w.n_d} + fp32 master/m/v")
+            f"rank {w.rank} shard of {n_valid:,} params, fp16 grads x{w.n_d} + {state}")
 
 
 def measured_peaks():
@@ -216,11 +217,13 @@ class ClockSampler:
 
 # --------------------------------------------------------------- cpu side ---
 
-def oracle_throughput(w, n_sample: int, seconds: float, threads: int):
+def oracle_throughput(w, n_sample: int, seconds: float, threads: int, optimizer: str = "adam"):
     """Time the oracle, as it stands, on a bounded sample of the workload:
     n_sample params of the rank's shard, split into contiguous chunks over
-    ``threads`` host threads (ctypes releases the GIL), steps repeated until
-    ``seconds`` have passed.  Returns (Gparams/s, steps, seconds, threads)."""
+    ``threads`` host threads (ctypes releases the GIL; 8-bit Adam chunks start
+    on its 2048-element blocks), steps repeated until ``seconds`` have passed.
+    ``optimizer`` picks the oracle's update: adam, sgd (momentum 0.9) or adam8.
+    Returns (Gparams/s, steps, seconds, threads)."""
     import numpy as np
     import oracle
     from zero_partitioned_mixed_partition_gb300 import synth
@@ -232,12 +235,31 @@ def oracle_throughput(w, n_sample: int, seconds: float, threads: int):
     m = np.zeros_like(master)
     v = np.zeros_like(master)
     params = np.zeros(n_sample, np.uint16)
+    blk = oracle.ADAM8_BLOCK
+    mc, vc = np.zeros(n_sample, np.uint8), np.zeros(n_sample, np.uint8)
+    ms, vs = np.zeros((n_sample + blk - 1) // blk, np.float32), np.zeros((n_sample + blk - 1) // blk, np.float32)
     bounds = np.linspace(0, n_sample, threads + 1).astype(np.int64)
+    if optimizer == "adam8":
+        bounds = np.minimum((bounds + blk - 1) // blk * blk, n_sample)
 
     def run_chunk(lo, hi, step):
-        oracle.shard_step([c[lo:hi] for c in contribs], master[lo:hi], m[lo:hi], v[lo:hi], params[lo:hi],
-                          lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
-                          loss_scale=w.loss_scale, step=step)
+        if hi <= lo:
+            return
+        if optimizer == "adam":
+            oracle.shard_step([c[lo:hi] for c in contribs], master[lo:hi], m[lo:hi], v[lo:hi], params[lo:hi],
+                              lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                              loss_scale=w.loss_scale, step=step)
+            return
+        g, bad = oracle.grad_reduce([c[lo:hi] for c in contribs], w.loss_scale)
+        if bad:
+            return
+        if optimizer == "sgd":
+            oracle.sgd_apply(g, master[lo:hi], m[lo:hi], params[lo:hi], lr=w.lr, momentum=0.9,
+                             weight_decay=w.weight_decay)
+        else:
+            oracle.adam8_apply(g, master[lo:hi], mc[lo:hi], vc[lo:hi], ms[lo // blk:(hi + blk - 1) // blk],
+                               vs[lo // blk:(hi + blk - 1) // blk], params[lo:hi], lr=w.lr, beta1=w.beta1,
+                               beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, step=step)
 
     steps, t0 = 0, time.perf_counter()
     while True:
@@ -252,6 +274,21 @@ def oracle_throughput(w, n_sample: int, seconds: float, threads: int):
         if el >= seconds:
             break
     return n_sample * steps / el / 1e9, steps, el, threads
+
+
+def oracle_sample(optimizer: str, full: int) -> int:
+    """Parameters the timed oracle sample holds (the 8-bit Adam oracle's
+    nearest-code search is the slowest per element)."""
+    return min(1_000_000 if optimizer == "adam8" else 4_000_000, full)
+
+
+def step_bytes_per_param(optimizer: str, n_d: int) -> float:
+    """Algorithmic HBM bytes per stepped parameter of the step kind."""
+    if optimizer == "sgd":
+        return 2 * n_d + 18
+    if optimizer == "adam8":
+        return 2 * n_d + 14 + 16 / 2048
+    return 2 * n_d + 26
 
 
 def native_cpu_throughput(w, n_sample: int, seconds: float, threads: int):
@@ -287,25 +324,25 @@ def reference_arm(args, rank: int):
     w = workload(args)
     elems = shard_elements(w)
     threads = os.cpu_count() or 1
-    n_sample = min(4_000_000, max(w.psi // w.n_d, 1))
+    n_sample = oracle_sample(args.optimizer, max(w.psi // w.n_d, 1))
     per_step_s = max(0.5, min(5.0, 60.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
-        oracle_throughput(w, n_sample, 0.0, threads)
+        oracle_throughput(w, n_sample, 0.0, threads, args.optimizer)
     vals = []
     t_all = time.perf_counter()
     for _ in range(args.steps):
-        g, steps, el, th = oracle_throughput(w, n_sample, per_step_s, threads)
+        g, steps, el, th = oracle_throughput(w, n_sample, per_step_s, threads, args.optimizer)
         vals.append(g)
         if time.perf_counter() - t_all > 180:
             break
     value = statistics.median(vals)
-    sample = (f"{n_sample:,} params of the rank's shard x N_d={w.n_d} contributions, "
+    sample = (f"{n_sample:,} params of the rank's shard x N_d={w.n_d} contributions, {args.optimizer} oracle, "
               f"{threads} threads over contiguous chunks, >= {per_step_s:.1f} s per step")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Gparams/s",
             "n_gpus": args.gpus, "steps": len(vals), "warmup": args.warmup,
             "ms_per_step": round(n_sample / (value * 1e9) * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": arm_config(args, w, elems, (26 + 2 * w.n_d) * elems, args.gpus),
+            "config": arm_config(args, w, elems, round(step_bytes_per_param(args.optimizer, w.n_d) * elems), args.gpus),
             "cpu_baseline": {"value": round(value, 4), "unit": "Gparams/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "Gparams/s", "h2d_bytes_per_step": 0,
@@ -531,15 +568,18 @@ def main():
         line["clip"] = clip_info
         line["roofline"]["kernel"] = "grad_norm_kernel + clipped_step_kernel"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        g, steps, el, th = oracle_throughput(w, min(4_000_000, elems), args.cpu_seconds, os.cpu_count() or 1)
+        opt = args.optimizer
+        ns = oracle_sample(opt, elems)
+        g, steps, el, th = oracle_throughput(w, ns, args.cpu_seconds, os.cpu_count() or 1, opt)
         line["cpu_baseline"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th, "kind": "oracle",
-                                "sample": f"{min(4_000_000, elems):,} params of the shard x N_d={w.n_d}, "
+                                "sample": f"{ns:,} params of the shard x N_d={w.n_d}, {opt} oracle, "
                                           f"{steps} steps in {el:.1f} s over {th} threads"}
-        g1, steps1, el1, _ = oracle_throughput(w, min(1_000_000, elems), 3.0, 1)
+        ns1 = min(ns // 4, elems)
+        g1, steps1, el1, _ = oracle_throughput(w, ns1, 3.0, 1, opt)
         line["cpu_baseline"]["single_thread"] = {
             "value": round(g1, 4), "unit": "Gparams/s", "cores": 1,
-            "sample": f"{min(1_000_000, elems):,} params x N_d={w.n_d}, {steps1} steps in {el1:.1f} s on one thread"}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            "sample": f"{ns1:,} params x N_d={w.n_d}, {opt} oracle, {steps1} steps in {el1:.1f} s on one thread"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.optimizer == "adam" and not clip:
         ns = min(32_000_000, elems)
         g, steps, el, th = native_cpu_throughput(w, ns, 3.0, os.cpu_count() or 1)
         line["cpu_native"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th,
