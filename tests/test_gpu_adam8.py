@@ -7,9 +7,9 @@ and params: bit-exact in the IEEE mode, within the stated tolerance in the
 fast one.  Cases: the 8- and 16-element layouts and the element-wise one
 (misaligned buffers), run-time and compile-time N_d, ragged blocks and
 tails, an overflow step (everything unchanged, loss scale halved), several
-shards in one call, and the full 1.5B-parameter shard on whole sampled
-blocks (blocks are independent, so the oracle steps each sampled block on
-its own)."""
+shards in one call, grouped launches, subnormal block scales, and the
+full-size 1.5B, 7.5B and ragged workloads on whole sampled blocks (blocks
+are independent, so the oracle steps each sampled block on its own)."""
 import numpy as np
 import pytest
 import torch
@@ -172,32 +172,42 @@ def test_adam8_multi_shard(zs, oracle, cuda_device):
             refs[r].compare(*_state(run, r, run.n_valid[r]), exact=True, what=f"shard {r} step {step}")
 
 
-def test_adam8_full_size_sampled_blocks(zs, oracle, cuda_device):
-    """The 1.5B-parameter, N_d = 4 shard (375,000,064 elements, the benchmark's
-    launch configuration and arithmetic mode) for two steps, checked on whole
-    blocks: the first, the last (partial) and 40 random ones.  Each block's
-    step depends only on its own elements, so the oracle steps them one by one."""
-    w = synth.WORKLOADS["xl"]
+@pytest.mark.parametrize("name", ["xl", "7b5", "ragged"])
+def test_adam8_full_size_sampled_blocks(zs, oracle, cuda_device, name):
+    """The full-size workloads in the benchmark's launch configuration and
+    arithmetic mode, two steps, checked on whole blocks: the first, the last
+    (partial) and 30 random ones of each checked shard (xl: 375,000,064
+    elements, N_d = 4, one-slot staged kernel; 7b5: 117,187,584, N_d = 64,
+    16-element kernel; ragged: all 16 shards in one grouped launch, shards 0,
+    7 and 15 checked).  Each block's step depends only on its own elements,
+    so the oracle steps them one by one."""
+    w = synth.WORKLOADS[name]
     run = WorkloadRunner(w, cuda_device, with_full_params=False, math=zs.ZS_MATH_FAST)
     run.enable_adam8()
-    r = run.shard_ids[0]
-    n = run.n_valid[r]
-    nb = (n + B - 1) // B
+    ids = run.shard_ids if len(run.shard_ids) == 1 else [run.shard_ids[i] for i in (0, 7, 15)]
     rng = np.random.Generator(np.random.PCG64(77))
-    blocks = sorted(set([0, nb - 1] + [int(b) for b in rng.integers(1, nb - 1, 40)]))
-    spans = [(b * B, min(n, (b + 1) * B)) for b in blocks]
-    refs = [OracleAdam8(oracle, to_np(run.state[r][0][0][lo:hi]), w) for lo, hi in spans]
-    hosts = [[synth.fp16_bits(g[lo:hi]) for g in run.grads[r]] for lo, hi in spans]
+    checks = []
+    for r in ids:
+        n = run.n_valid[r]
+        nb = (n + B - 1) // B
+        blocks = sorted(set([0, nb - 1] + [int(b) for b in rng.integers(1, nb - 1, 30)]))
+        for b in blocks:
+            lo, hi = b * B, min(n, (b + 1) * B)
+            ref = OracleAdam8(oracle, to_np(run.state[r][0][0][lo:hi]), w)
+            host = [synth.fp16_bits(g[lo:hi]) for g in run.grads[r]]
+            checks.append((r, b, lo, hi, ref, host))
     for step in (1, 2):
         run.step_adam8()
         torch.cuda.synchronize()
-        master, mc, vc, ms, vs, params = run.current_adam8(r)
-        for b, (lo, hi), ref, host in zip(blocks, spans, refs, hosts):
+        state = {r: run.current_adam8(r) for r in ids}
+        for r, b, lo, hi, ref, host in checks:
+            master, mc, vc, ms, vs, params = state[r]
             g, bad = ref.reduce(host, w.loss_scale)
             assert not bad
             ref.apply(g, step)
             ref.compare(to_np(master[lo:hi]), to_np(mc[lo:hi]), to_np(vc[lo:hi]), to_np(ms[b:b + 1]),
-                        to_np(vs[b:b + 1]), f16_bits(params[lo:hi]), exact=False, what=f"xl block {b} step {step}")
+                        to_np(vs[b:b + 1]), f16_bits(params[lo:hi]), exact=False,
+                        what=f"{name} shard {r} block {b} step {step}")
 
 
 @pytest.mark.parametrize("n_d", [4, 16])

@@ -430,16 +430,18 @@ adam8_step_kernel(const __grid_constant__ A8Args<CAP, G> p) {
         // phases so that the bias corrections can use the exact division below
         float m[VEC], v[VEC];
         float low = 1.0f;  // smallest |m'|, v' of this thread's share
+        float nfs = 0.0f;  // sum of acc * 0: NaN once some acc is +-inf or NaN, else 0
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             const float g = __fmul_rn(acc[j], c.inv);
-            bad |= nonfinite(acc[j]) ? 1u : 0u;
+            nfs = __fmaf_rn(acc[j], 0.0f, nfs);
             m[j] = __fadd_rn(__fmul_rn(c.b1, __fmul_rn(sm.dec7[cm[j]], scale_m)), __fmul_rn(c.c1, g));
             v[j] = __fadd_rn(__fmul_rn(c.b2, __fmul_rn(sm.mag8[cv[j]], scale_v)), __fmul_rn(c.c2, __fmul_rn(g, g)));
             low = fminf(low, fminf(fabsf(m[j]), v[j]));
         }
         // m' / (1 - beta1^t), v' / (1 - beta2^t): exact by two corrections,
         // unless a warp holds a value below 2^-100 (or 0): then IEEE divisions
+        bad |= (nfs != nfs) ? 1u : 0u;  // the non-finite test of this share
         float mh[VEC], vh[VEC];
         if (__any_sync(0xffffffffu, !(low >= 0x1p-100f))) {  // (warp-uniform)
 #pragma unroll
@@ -580,9 +582,11 @@ int a8_blocks(const void* kernel, int threads, size_t smem, int64_t nq) {
     return (int)(nq < full ? (nq < 1 ? 1 : nq) : full);
 }
 
-// Contributions up to which the staged kernel is used (its two stages take
-// 2 (4096 N_d + 12288) bytes of shared memory per CTA).
-constexpr int kStagedMaxNd = 8;
+// Contributions up to which the staged kernel is used: its two stages take
+// 2 (4096 N_d + 12288) bytes of shared memory per CTA, 57 KB at N_d = 4 (three
+// CTAs per SM).  At N_d = 8 they would allow only two, and the direct kernel
+// measured faster (gpt2s workload: 134.6 against 129.9 Gparams/s).
+constexpr int kStagedMaxNd = 4;
 
 template <int CAP, int G, int VEC, int ND, bool FAST, bool VECLOAD, bool STAGED>
 int32_t launch_a8(const A8Args<CAP, G>& a, cudaStream_t stream) {
@@ -629,11 +633,11 @@ int32_t launch_a8_cap(const zs_adam8_shard* shards, int count, int32_t n_d, int 
     a.flag = &ctrl->overflow;
     a.maps = host_maps().maps;
     const bool fast = hp.math == ZS_MATH_FAST;
-    // Up to 8 contributions: the staged 8-element kernel.  9-16: the direct
+    // Up to 4 contributions: the staged 8-element kernel.  5-16: the direct
     // 8-element kernel, whose contribution loads already keep enough bytes in
     // flight (ragged workload, N_d = 16: 128.0 Gparams/s against 124.9 for the
     // 16-element kernel).  Above 16: the 16-element kernel.
-    if constexpr (ND == 0 && CAP <= 16) {
+    if constexpr (ND == 0 && CAP <= kStagedMaxNd) {
         if (width >= 1 && n_d <= kStagedMaxNd)
             return fast ? launch_a8<CAP, G, 8, ND, true, true, true>(a, stream)
                         : launch_a8<CAP, G, 8, ND, false, true, true>(a, stream);
