@@ -488,9 +488,10 @@ typedef struct zs_adam8_shard {
  *   scale is 0) clamped to [-1, 1], ties to the smaller magnitude, sign bit for
  *   a negative x with a non-zero magnitude code; v alike.
  * hp->math applies to u as in zero_shard_step; the codes do not depend on it.
- * One kernel launch per shard with n > 0, then the device commit (a skipped
- * step leaves set cur, so codes and scales too, untouched).  Per element
- * 2 n_d + 14 bytes (+ 16 per block).
+ * Consecutive shards of one access width (empty shards join any group) are
+ * stepped up to 16 per launch with n_d <= 64, one per launch above; then the
+ * device commit (a skipped step leaves set cur, so codes and scales too,
+ * untouched).  Per element 2 n_d + 14 bytes (+ 16 per block).
  * Source: "DeepSpeed ZeRO Stages", sec. 1.2 (8-bit Adam, K = 6), with the update of "ZeRO Stage 1
  * Math", "The per-step mechanics", beats 2-3. */
 ZS_API int32_t zero_shard_step_adam8_async(const zs_adam8_shard* shards, int32_t n_shards, int32_t n_d,

@@ -11,10 +11,12 @@
 // against the block's new largest magnitude.
 //
 // One CTA owns one 2048-element block per loop iteration (256 threads x 8
-// elements, or 128 x 16 when N_d > 4), so the block's absmax is one warp
+// elements, or 128 x 16 when N_d > 16), so the block's absmax is one warp
 // shuffle reduction plus one CTA barrier, and the quantization happens in
 // registers: every state byte is read once and written once.  Per element
 // 2 N_d + 6 bytes are read and 8 written (+ 16 bytes per block for the scales).
+// One launch steps up to 16 shards of a step, their blocks back to back; up to
+// N_d = 4 each thread prefetches its share of the next block with cp.async.
 //
 // The nearest-code search: the map values, and for each pair of neighbours the
 // largest float not above their midpoint (so `x > t` decides "nearer to the
