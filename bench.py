@@ -134,7 +134,7 @@ def measured_peaks():
 # the sources that kernel is compiled from (the record holds their digest).
 TRAFFIC_RECORDS = {
     "adam": ("shard_step_kernel_traffic.txt", ("shard_step.cu", "step_common.cuh")),
-    "adam8": ("adam8_step_kernel_traffic.txt", ("adam8.cu", "step_common.cuh")),
+    "adam8": ("adam8_step_kernel_traffic.txt", ("adam8.cu", "adam8_math.cuh", "step_common.cuh")),
 }
 
 
