@@ -164,6 +164,27 @@ def recorded_traffic(kind: str = "adam"):
         return None
 
 
+def recorded_instructions(kind: str):
+    """Thread instructions per stepped parameter from the same record (keyed
+    by N_d), valid only while the kernel sources are unchanged (else None)."""
+    path = os.path.join(ROOT, "profiles", TRAFFIC_RECORDS[kind][0])
+    try:
+        vals = dict(line.split(":", 1) for line in open(path) if ":" in line and not line.startswith("#"))
+        vals = {k.strip(): v.strip() for k, v in vals.items()}
+        if vals.get("kernel_source_sha256_16") != kernel_source_digest(kind):
+            return None
+        return {int(k.split("_")[-1]): float(v) for k, v in vals.items()
+                if k.startswith("thread_instructions_per_param_nd_")}
+    except Exception:
+        return None
+
+
+# Peak instruction issue of the GPU: 152 SMs x 4 schedulers x 32 lanes at the
+# 2070 MHz maximum SM clock (the clock the timed runs hold), thread
+# instructions per second.
+ISSUE_PEAK_TINSTR_S = 152 * 4 * 32 * 2.07e9
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -558,6 +579,15 @@ def main():
         line["optimizer"] = {"kind": "sgd", "momentum": 0.9, "timed": "fused kernel + commit"}
         line["roofline"]["kernel"] = ("sgd_group_kernel" if len(run.views) > 1 else "sgd_step_kernel") + " + commit_kernel"
     if args.optimizer == "adam8":
+        instr = recorded_instructions("adam8")
+        if instr and w.n_d in instr:
+            # the N_d <= 4 kernel is bound by instruction issue, not HBM: its
+            # issue roofline, from the ncu-counted instructions per parameter
+            rate = instr[w.n_d] * elems / (mean_kern_ms / 1e3)
+            line["roofline_issue"] = {"bound": "alu", "achieved": round(rate / 1e12, 3),
+                                      "peak": round(ISSUE_PEAK_TINSTR_S / 1e12, 3), "unit": "T thread-instr/s",
+                                      "frac": round(rate / ISSUE_PEAK_TINSTR_S, 4),
+                                      "instructions_per_param": instr[w.n_d], "source": "ncu, recorded"}
         line["optimizer"] = {"kind": "adam8", "block": binding.ZS_ADAM8_BLOCK,
                              "state": "fp32 master, uint8 codes of m and v, fp32 scale per block (ping-pong)",
                              "timed": "fused kernel per shard + commit"}
