@@ -464,7 +464,7 @@ ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shard
  * The state value is map[code] * scale; codes and scales all 0 are m = v = 0
  * (the state before the first step).  With grads and params 16-byte aligned,
  * master 16-byte and the codes 8-byte aligned a thread moves 8 elements per
- * access (16 with n_d > 4 and master 32-byte, codes 16-byte aligned); other
+ * access (16 with n_d > 16 and master 32-byte, codes 16-byte aligned); other
  * naturally aligned buffers take element-wise accesses, same arithmetic. */
 typedef struct zs_adam8_shard {
     const uint16_t* const* grads;
