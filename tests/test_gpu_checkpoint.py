@@ -46,3 +46,47 @@ def test_save_load_resume_is_exact(zs, cuda_device, n_d):
     assert a == b and a["step"] == 4 and a["skipped"] == 1 and a["loss_scale"] == 512.0
     for x, y in zip(straight.current(0), resumed.current(0)):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("n_d", [4, 16])
+def test_adam8_save_load_resume_is_exact(zs, cuda_device, n_d):
+    """The same with 8-bit Adam state: the committed codes and block scales
+    travel with the checkpoint, and 3 + 2 steps equal 5 straight steps bit for
+    bit (codes, scales, master, params, control block)."""
+    n = 2048 * 9 + 5
+    w = synth.Workload(name="ckpt8", numels=(n * n_d,), n_d=n_d, rank=0, align=1, steps=5, lr=1e-3, beta1=0.9,
+                       beta2=0.999, eps=1e-8, weight_decay=0.01, loss_scale=1024.0, grad_dist="normal",
+                       grad_std=1e-2, grad_mult=1024.0, grads_fresh_per_step=True, master_dist="normal",
+                       master_param=0.02, seed=41 + n_d)
+
+    def runner():
+        run = WorkloadRunner(w, cuda_device)
+        run.enable_adam8()
+        return run
+
+    def run_steps(run, steps):
+        for s in steps:
+            run.refresh_grads(s)
+            if s == 2:
+                run.grads[0][0][7] = float("nan")        # step 2 overflows and is skipped
+            run.step_adam8()
+        torch.cuda.synchronize()
+
+    straight = runner()
+    run_steps(straight, [1, 2, 3, 4, 5])
+    first = runner()
+    run_steps(first, [1, 2, 3])
+    ckpt = first.save()
+    del first
+    resumed = runner()
+    for pair in resumed.adam8[0]:                # scribble over the fresh 8-bit state: load must replace it
+        for t in pair:
+            t.fill_(3)
+    resumed.step_adam8()
+    torch.cuda.synchronize()
+    resumed.load(ckpt)
+    run_steps(resumed, [4, 5])
+    a, b = straight.ctrl_host(), resumed.ctrl_host()
+    assert a == b and a["step"] == 4 and a["skipped"] == 1
+    for x, y in zip(straight.current_adam8(0), resumed.current_adam8(0)):
+        assert torch.equal(x, y)

@@ -205,13 +205,17 @@ class WorkloadRunner:
     def save(self) -> dict:
         """Host copy of everything a resumed run needs: the control block's
         bytes (loss scale, t, beta^t, ping-pong set, counters) and, per shard,
-        the committed master/m/v and the fp16 slice.  Call with the stream idle."""
+        the committed master/m/v and the fp16 slice -- plus, with 8-bit Adam
+        state (enable_adam8), its committed codes and block scales.  Call with
+        the stream idle."""
         torch.cuda.synchronize(self.device)
         cur = self.ctrl_host()["cur"]
         out = {"ctrl": self.ctrl.detach().cpu().clone(), "shards": {}}
         for r in self.shard_ids:
             master, m, v, params = self.state[r]
             out["shards"][r] = tuple(t.detach().cpu().clone() for t in (master[cur], m[cur], v[cur], params))
+        if getattr(self, "adam8", None):
+            out["adam8"] = {r: tuple(pair[cur].detach().cpu().clone() for pair in self.adam8[r]) for r in self.shard_ids}
         return out
 
     def load(self, ckpt: dict):
@@ -227,6 +231,12 @@ class WorkloadRunner:
             dmm[cur].copy_(m.to(self.device))
             dv[cur].copy_(v.to(self.device))
             dp.copy_(params.to(self.device))
+        if "adam8" in ckpt:
+            if not getattr(self, "adam8", None):
+                raise RuntimeError("the checkpoint holds 8-bit Adam state: call enable_adam8() first")
+            for r, saved in ckpt["adam8"].items():
+                for pair, t in zip(self.adam8[r], saved):
+                    pair[cur].copy_(t.to(self.device))
         torch.cuda.synchronize(self.device)
 
     # ------------------------------------------------------------ accounting --
