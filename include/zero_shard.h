@@ -483,10 +483,10 @@ typedef struct zs_adam8_shard {
  *   m = +-mag7[m_code & 127] * m_scale,   v = mag8[v_code] * v_scale
  *   m', v', theta' and params = fp16_rn(theta') as in zero_shard_step
  *   m_scale' = max |m'| and v_scale' = max v' over the block
- *   m_code' = the code of the map value nearest to x = m' * r, r the fp32
- *   reciprocal of m_scale' (correctly rounded, once per block; x = 0 when the
- *   scale is 0) clamped to [-1, 1], ties to the smaller magnitude, sign bit for
- *   a negative x with a non-zero magnitude code; v alike.
+ *   m_code' = the code of the map value nearest to x = m' / m_scale' (the
+ *   quotient rounded once to fp32, as an IEEE division rounds it; x = 0 when
+ *   the scale is 0), ties to the smaller magnitude, sign bit for a negative x
+ *   with a non-zero magnitude code; v alike.
  * hp->math applies to u as in zero_shard_step; the codes do not depend on it.
  * Consecutive shards of one access width (empty shards join any group) are
  * stepped up to 16 per launch with n_d <= 64, one per launch above; then the

@@ -79,7 +79,9 @@
  *     m and v after Dettmers et al. (blocks of 2048, absmax scale, nearest
  *     code of a decimal-exponent map, signed for m and unsigned for v, ties
  *     to the smaller magnitude), fp32 master; the map's fraction values are
- *     the upper ends of their steps so that x = 1 is exact;
+ *     the upper ends of their steps so that x = 1 is exact; the state is
+ *     normalized as the method states it, state / absmax, one IEEE fp32
+ *     division per element;
  *
  * Parity pins for every function live in the tests (closed forms and worked
  * values printed on the pages, exhaustive fp16 checks against numpy, the
@@ -530,9 +532,8 @@ static int oracle_nearest(float a, const float* table, int count)
     return best;
 }
 
-/* Code of x under the signed map: bit 7 set for x < 0 (unless the magnitude
- * code is 0), bits 0-6 the code of |x| in mag7.  (x lies in [-1, 1] up to
- * one rounding of the scale's reciprocal.) */
+/* Code of x in [-1, 1] under the signed map: bit 7 set for x < 0 (unless the
+ * magnitude code is 0), bits 0-6 the code of |x| in mag7. */
 uint8_t oracle_adam8_code_signed(float x, const float* mag7)
 {
     int k = oracle_nearest(fabsf(x), mag7, 128);
@@ -552,8 +553,9 @@ uint8_t oracle_adam8_code_unsigned(float x, const float* mag8)
  *   m   = (+-mag7[code & 127]) * sm      v = mag8[code] * sv
  *   m', v', theta' and the fp16 cast as in oracle_adam_apply
  *   sm' = max |m'| over the block        sv' = max v' over the block
- *   codes of x = m' * (1 / sm') and v' * (1 / sv'), the reciprocal of each
- *   scale rounded once to fp32 (0 when the scale is 0), x clamped to [-1, 1]
+ *   codes of x = m' / sm' and v' / sv', each one IEEE fp32 division (x = 0
+ *   when the scale is 0); the division is monotone and sm' / sm' = 1, so x
+ *   never leaves [-1, 1] and needs no clamp
  * Codes 0 with scale 0 stand for m = v = 0 before the first step. */
 int32_t oracle_adam8_apply(const float* g, int64_t n, float* master, uint8_t* m_codes, uint8_t* v_codes,
                            float* m_scale, float* v_scale, uint16_t* params, double lr, double beta1,
@@ -602,16 +604,9 @@ int32_t oracle_adam8_apply(const float* g, int64_t n, float* master, uint8_t* m_
             if (fabsf(mj) > amax_m) amax_m = fabsf(mj);
             if (vj > amax_v) amax_v = vj;
         }
-        float inv_m = amax_m > 0.0f ? 1.0f / amax_m : 0.0f;
-        float inv_v = amax_v > 0.0f ? 1.0f / amax_v : 0.0f;
         for (int64_t j = lo; j < hi; ++j) {
-            float xm = m_new[j - lo] * inv_m;
-            float xv = v_new[j - lo] * inv_v;
-            /* |x| exceeds 1 only by the reciprocal's rounding, or without bound
-             * when a scale below 2^-126 has no finite reciprocal: clamp */
-            if (xm > 1.0f) xm = 1.0f;
-            if (xm < -1.0f) xm = -1.0f;
-            if (xv > 1.0f) xv = 1.0f;
+            float xm = amax_m > 0.0f ? m_new[j - lo] / amax_m : 0.0f;
+            float xv = amax_v > 0.0f ? v_new[j - lo] / amax_v : 0.0f;
             m_codes[j] = oracle_adam8_code_signed(xm, mag7);
             v_codes[j] = oracle_adam8_code_unsigned(xv, mag8);
         }

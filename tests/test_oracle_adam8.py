@@ -10,10 +10,16 @@ What fixes the oracle here, apart from itself:
   - reduction to the pinned fp32 Adam: the first step from a zero state, and
     every step of blocks whose states have one magnitude (x = +-1 is exact);
   - the decomposition dequantize -> fp32 Adam -> block absmax -> nearest code
-    of m' * (1 / absmax), checked against the pinned fp32 Adam and a
-    brute-force nearest search;
+    of m' / absmax, checked against the pinned fp32 Adam and a brute-force
+    nearest search;
+  - the normalization is the quotient m' / absmax rounded once: two blocks
+    worked out in exact rational arithmetic where m' * fp32(1 / absmax) lands
+    on the other side of a code threshold (a reciprocal-multiply reading
+    fails them);
   - block isolation: a spike in one block of 2048 leaves the others alone.
 """
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -172,10 +178,8 @@ def test_step_is_dequantize_adam_quantize(oracle):
     for b in range(ms.size):
         sl = blk == b
         assert ms[b] == np.abs(m[sl]).max() and vs[b] == v[sl].max()
-    inv_m = (np.float32(1) / ms).astype(np.float32)                   # one fp32 reciprocal per block
-    inv_v = (np.float32(1) / vs).astype(np.float32)
-    xm = (m * inv_m[blk]).astype(np.float32).astype(np.float64)
-    xv = (v * inv_v[blk]).astype(np.float32).astype(np.float64)
+    xm = (m / ms[blk]).astype(np.float32).astype(np.float64)          # one IEEE fp32 division each
+    xv = (v / vs[blk]).astype(np.float32).astype(np.float64)
     dm = np.abs(np.abs(xm)[:, None] - mag7[None, :])
     dv = np.abs(xv[:, None] - mag8[None, :])
     km = np.argmin(dm, axis=1)                                         # first minimum: the smaller magnitude
@@ -206,10 +210,86 @@ def test_blocks_are_independent(oracle):
     assert not np.array_equal(a_mc[B:2 * B], b_mc[B:2 * B])
 
 
-def test_scale_without_finite_reciprocal_clamps(oracle):
-    """A block whose moments decayed below 2^-126: 1 / scale overflows to inf,
-    x = m' * inf is clamped to +-1, so every non-zero m' (v') gets the top
-    code and every zero one code 0; the stored scale stays the block max."""
+def _rn32(q: Fraction) -> np.float32:
+    """The float32 nearest to the rational q (ties to the even significand),
+    found among the neighbours of a first guess by exact distances."""
+    f = np.float32(float(q))
+    cands = [f, np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(-np.inf))]
+    def key(c):
+        return (abs(Fraction(float(c)) - q), int(np.array(c).view(np.uint32)) & 1)
+    return min(cands, key=key)
+
+
+def _nearest(a: np.float32, table) -> int:
+    """Index of the table value nearest to a, by exact distances; ties to the smaller."""
+    d = [abs(Fraction(float(a)) - Fraction(float(t))) for t in table]
+    return d.index(min(d))
+
+
+def test_normalization_is_the_ieee_quotient(oracle):
+    """Two blocks, worked out by hand and checked here in exact rational
+    arithmetic, where normalizing by a rounded reciprocal crosses a code
+    threshold that the quotient itself does not.  First step from a zero
+    state with beta1 = beta2 = 0.5, so m' = g / 2 and v' = fp32(g^2) / 2 are
+    known exactly.
+
+    Block 0 (the signed map, m): g = [2 s, 2 x], s = 0x3c0185d6
+    (0.0079054441), x = 0x3bd9272f (0.0066269855).  m' = [s, x], scale s.
+    The exact x / s = 0.838281239140 lies below 0.838281244040, the midpoint
+    of mag7[115] = 0.831250012 and mag7[116] = 0.845312476; rounded once it
+    is 0x3f569999 = 0.838281214237, still below: code 115.  fp32(1 / s) =
+    0x42fcfd7f = 126.495109558 is 2.1e-8 (relative) above 1 / s, and
+    x * fp32(1 / s) rounds to 0x3f56999a = 0.838281273842, above the
+    midpoint: a reciprocal-multiply normalization would store code 116.
+
+    Block 1 (the unsigned map, v): g = [ga, gb], ga = 0x3af8485f
+    (0.0018942467), gb = 0x3ae79282 (0.0017667564).  v' = fp32(g^2) / 2,
+    scale v'[0].  The exact quotient 0.869921888688 lies below
+    0.869921892881, the midpoint of mag8[236] and mag8[237]; rounded once it
+    is 0x3f5eb333 = 0.869921863079: code 236.  The reciprocal product is
+    0x3f5eb334 = 0.869921922684: code 237.
+    """
+    mag7, mag8 = oracle.adam8_maps()
+    f32 = lambda bits: np.array([bits], np.uint32).view(np.float32)[0]
+    s, x = f32(0x3C0185D6), f32(0x3BD9272F)
+    ga, gb = f32(0x3AF8485F), f32(0x3AE79282)
+    n = 2 * B
+    g = np.zeros(n, np.float32)
+    g[0], g[1] = 2 * s, 2 * x                                          # exact doublings
+    g[B], g[B + 1] = ga, gb
+    master = np.zeros(n, np.float32)
+    mc, vc, ms, vs = _state(n)
+    oracle.adam8_apply(g, master, mc, vc, ms, vs, None, lr=1e-3, beta1=0.5, beta2=0.5, eps=1e-8,
+                       weight_decay=0.0, step=1)
+
+    # block 0, m: the scale and the code of x / s, all in exact arithmetic
+    assert ms[0] == s
+    q = Fraction(float(x)) / Fraction(float(s))
+    k = _nearest(_rn32(q), mag7)
+    mid = (Fraction(float(mag7[115])) + Fraction(float(mag7[116]))) / 2
+    assert k == 115 and q < mid and Fraction(float(_rn32(q))) <= mid
+    rcp = _rn32(Fraction(1) / Fraction(float(s)))
+    assert _nearest(_rn32(Fraction(float(x)) * Fraction(float(rcp))), mag7) == 116   # the pin discriminates
+    assert mc[0] == 127 and mc[1] == 115
+
+    # block 1, v: v' = fp32(g^2) / 2 (the halving is exact)
+    va = _rn32(Fraction(float(ga)) ** 2) / np.float32(2)
+    vb = _rn32(Fraction(float(gb)) ** 2) / np.float32(2)
+    assert vs[1] == va
+    q = Fraction(float(vb)) / Fraction(float(va))
+    mid = (Fraction(float(mag8[236])) + Fraction(float(mag8[237]))) / 2
+    assert _nearest(_rn32(q), mag8) == 236 and q < mid
+    rcp = _rn32(Fraction(1) / Fraction(float(va)))
+    assert _nearest(_rn32(Fraction(float(vb)) * Fraction(float(rcp))), mag8) == 237
+    assert vc[B] == 255 and vc[B + 1] == 236
+
+
+def test_subnormal_scales(oracle):
+    """A block whose moments decayed below 2^-126: the quotient m' / scale is
+    still formed (a subnormal divided by a subnormal), so the block maximum
+    keeps the top code and every other element the code nearest to its exact
+    quotient rounded once -- checked in rational arithmetic; the stored
+    scale is the block max."""
     mag7, mag8 = oracle.adam8_maps()
     rng = np.random.Generator(np.random.PCG64(12))
     n = B
@@ -217,6 +297,7 @@ def test_scale_without_finite_reciprocal_clamps(oracle):
     vc = rng.integers(0, 256, n).astype(np.uint8)
     mc[:10] = 0                                                       # zero moments stay zero
     vc[:10] = 0
+    mc[10], vc[10] = 0x7F, 0xFF                                       # one element at the block max
     ms = np.array([1e-39], np.float32)                                # subnormal scales
     vs = np.array([1e-39], np.float32)
     m_old, v_old = _decode(oracle, mc, vc, ms, vs)
@@ -226,8 +307,10 @@ def test_scale_without_finite_reciprocal_clamps(oracle):
     m_new = np.float32(HP["beta1"]) * m_old                           # g = 0: m' = b1 m, v' = b2 v
     v_new = np.float32(HP["beta2"]) * v_old
     assert ms[0] == np.abs(m_new).max() and vs[0] == v_new.max()
-    with np.errstate(over="ignore"):
-        assert np.isinf(np.float32(1) / ms[0]) and np.isinf(np.float32(1) / vs[0])
-    want_m = np.where(m_new == 0, 0, np.where(m_new < 0, 0xFF, 0x7F)).astype(np.uint8)
-    want_v = np.where(v_new == 0, 0, 0xFF).astype(np.uint8)
-    assert np.array_equal(mc, want_m) and np.array_equal(vc, want_v)
+    assert mc[10] == 0x7F and vc[10] == 0xFF
+    sm, sv = Fraction(float(ms[0])), Fraction(float(vs[0]))
+    for j in range(0, n, 7):
+        km = _nearest(_rn32(Fraction(float(abs(m_new[j]))) / sm), mag7)
+        want_m = (0x80 | km) if (m_new[j] < 0 and km > 0) else km
+        assert mc[j] == want_m, j
+        assert vc[j] == _nearest(_rn32(Fraction(float(v_new[j])) / sv), mag8), j
