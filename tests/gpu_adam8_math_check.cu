@@ -9,6 +9,12 @@
 //  2. div_by_constant, for every float x with 2^-100 <= |x| < 2^100 (both
 //     signs) and 40 divisors d = 1 - beta^t formed as the step forms them,
 //     against CUDA's IEEE division __fdiv_rn(x, d), bit for bit.
+//  3. the normalization of a block by its scale: for 40 scales d with
+//     scale_divisor_ok(d) (ends of the range, 1 and its neighbours, two
+//     scales from the oracle's pins, 33 spread over [2^-64, 2^64]) and every
+//     float x with |x| <= d (both signs), the codes of div_by_constant(x, d,
+//     RN(1/d)) under both maps equal the codes of __fdiv_rn(x, d), and the two
+//     quotients are equal bit for bit wherever |x / d| >= 2^-27.
 //
 // Every loop is a grid-stride loop over a fixed range; nothing waits.  Prints
 // one line per check and exits 1 if any value differs.
@@ -69,6 +75,45 @@ __global__ void div_check(float d, uint32_t lo, uint32_t hi, Result* out) {
         const float q1 = div_by_constant(x, d, y), r1 = __fdiv_rn(x, d);
         const float q2 = div_by_constant(-x, d, y), r2 = __fdiv_rn(-x, d);
         if (__float_as_uint(q1) != __float_as_uint(r1) || __float_as_uint(q2) != __float_as_uint(r2)) {
+            atomicAdd(&out->bad, 1ull);
+            atomicMin(&out->first, (unsigned long long)b);
+        }
+    }
+}
+
+// the sign-and-magnitude code of the signed map, as the step forms it
+__device__ __forceinline__ uint32_t signed_code(float x, const float* thr, const uint8_t* bucket) {
+    const uint32_t k = nearest_code(fabsf(x), thr, bucket);
+    return (x < 0.0f && k > 0u) ? (k | 0x80u) : k;
+}
+
+__global__ void scale_check(float d, const float* thr7, const uint8_t* b7, const float* thr8, const uint8_t* b8,
+                            Result* out) {
+    __shared__ float s_thr7[128], s_thr8[256];
+    __shared__ uint8_t s_b7[kBuckets], s_b8[kBuckets];
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        if (i < 128) s_thr7[i] = thr7[i];
+        s_thr8[i] = thr8[i];
+    }
+    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) {
+        s_b7[i] = b7[i];
+        s_b8[i] = b8[i];
+    }
+    __syncthreads();
+    const float y = __frcp_rn(d);
+    const uint64_t hi = __float_as_uint(d);  // every float in [0, d]
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t b = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; b <= hi; b += stride) {
+        const float x = __uint_as_float((uint32_t)b);
+        bool bad = false;
+        for (int sgn = 0; sgn < 2; ++sgn) {
+            const float xs = sgn ? -x : x;
+            const float q = div_by_constant(xs, d, y), r = __fdiv_rn(xs, d);
+            if (fabsf(r) >= 0x1p-27f && __float_as_uint(q) != __float_as_uint(r)) bad = true;
+            if (signed_code(q, s_thr7, s_b7) != signed_code(r, s_thr7, s_b7)) bad = true;
+            if (nearest_code(fabsf(q), s_thr8, s_b8) != nearest_code(fabsf(r), s_thr8, s_b8)) bad = true;
+        }
+        if (bad) {
             atomicAdd(&out->bad, 1ull);
             atomicMin(&out->first, (unsigned long long)b);
         }
@@ -143,6 +188,33 @@ int main() {
             snprintf(name, sizeof(name), "div_by_constant, d = 1 - %g^%d = %.9g, 2^-100 <= |x| < 2^100", beta, t, d);
             run(name, [&] { div_check<<<blocks, threads>>>(d, lo, hi, d_res); });
         }
+    // block scales: the range ends, 1 and its neighbours, two scales of the
+    // oracle's normalization pins, and 33 spread over the range with
+    // mantissas from a fixed linear congruential sequence
+    float *d_thr7, *d_thr8;
+    uint8_t *d_b7, *d_b8;
+    if (cudaMalloc(&d_thr7, 128 * 4) || cudaMalloc(&d_thr8, 256 * 4) || cudaMalloc(&d_b7, kBuckets) ||
+        cudaMalloc(&d_b8, kBuckets))
+        return fail("cudaMalloc");
+    cudaMemcpy(d_thr7, thr7, 128 * 4, cudaMemcpyHostToDevice);
+    cudaMemcpy(d_thr8, thr8, 256 * 4, cudaMemcpyHostToDevice);
+    cudaMemcpy(d_b7, b7, kBuckets, cudaMemcpyHostToDevice);
+    cudaMemcpy(d_b8, b8, kBuckets, cudaMemcpyHostToDevice);
+    uint32_t scales[40] = {(127u - 64u) << 23, (127u + 64u) << 23, 0x3f800000u, 0x3f800001u, 0x3f7fffffu,
+                           0x3c0185d6u, 0x35f0cc4du};
+    uint32_t lcg = 12345u;
+    for (int i = 7; i < 40; ++i) {
+        lcg = lcg * 1664525u + 1013904223u;
+        const uint32_t e = (uint32_t)(127 - 64 + (i - 7) * 127 / 32);   // exponents -64 .. 63
+        scales[i] = (e << 23) | (lcg >> 9);
+    }
+    for (uint32_t bits : scales) {
+        float d;
+        std::memcpy(&d, &bits, 4);
+        char name[96];
+        snprintf(name, sizeof(name), "block quotient, scale 0x%08x = %.9g, every |x| <= scale", bits, d);
+        run(name, [&] { scale_check<<<blocks, threads>>>(d, d_thr7, d_b7, d_thr8, d_b8, d_res); });
+    }
     if (cudaDeviceSynchronize() != cudaSuccess) return fail("kernels");
     printf("%s\n", status == 0 ? "all equal" : "MISMATCH");
     return status;

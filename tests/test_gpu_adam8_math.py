@@ -6,7 +6,11 @@ program tests/gpu_adam8_math_check.cu (compiled here for sm_103a):
   distances, ties to the smaller), for every float in [0, 1], both maps;
 - the constant-divisor division (correctly rounded reciprocal, two residual
   corrections) against CUDA's IEEE division, bit for bit, for every float
-  2^-100 <= |x| < 2^100 and 40 divisors 1 - beta^t."""
+  2^-100 <= |x| < 2^100 and 40 divisors 1 - beta^t;
+- the normalization of a block by its scale (the same division by the
+  block's largest magnitude) against the IEEE quotient: equal codes under
+  both maps for every |x| <= scale, equal quotients wherever they reach a
+  code threshold, for 40 scales over [2^-64, 2^64]."""
 import os
 import shutil
 import subprocess
@@ -29,4 +33,4 @@ def test_adam8_math_exhaustive(cuda_device, tmp_path):
     print(r.stdout)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("all equal")
-    assert r.stdout.count("0 mismatches") == 4 + 40
+    assert r.stdout.count("0 mismatches") == 4 + 40 + 40

@@ -403,16 +403,30 @@ adam8_step_kernel(const __grid_constant__ A8Args<CAP, G> p) {
             am = fmaxf(am, s_red[par][0][w]);
             av = fmaxf(av, s_red[par][1][w]);
         }
-        // codes of m' * (1 / am) and v' * (1 / av), one rounded reciprocal per block
-        const float rm = am > 0.0f ? __frcp_rn(am) : 0.0f;
-        const float rv = av > 0.0f ? __frcp_rn(av) : 0.0f;
+        // codes of x = m' / am and v' / av, each quotient rounded once: by the
+        // constant-divisor division when both scales allow it (the block's
+        // scales are the same in every thread, so the branch is uniform), else
+        // by IEEE divisions; x = 0 for a zero scale
+        float xm[VEC], xv[VEC];
+        if (scale_divisor_ok(am) && scale_divisor_ok(av)) {
+            const float rm = __frcp_rn(am), rv = __frcp_rn(av);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                xm[j] = div_by_constant(m[j], am, rm);
+                xv[j] = div_by_constant(v[j], av, rv);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                xm[j] = am > 0.0f ? __fdiv_rn(m[j], am) : 0.0f;
+                xv[j] = av > 0.0f ? __fdiv_rn(v[j], av) : 0.0f;
+            }
+        }
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            const float xm = __fmul_rn(m[j], rm);
-            const float xv = __fmul_rn(v[j], rv);
-            const uint32_t k = nearest_code(fabsf(xm), sm.thr7, sm.bucket7);
-            cm[j] = (xm < 0.0f && k > 0u) ? (k | 0x80u) : k;
-            cv[j] = nearest_code(fabsf(xv), sm.thr8, sm.bucket8);
+            const uint32_t k = nearest_code(fabsf(xm[j]), sm.thr7, sm.bucket7);
+            cm[j] = (xm[j] < 0.0f && k > 0u) ? (k | 0x80u) : k;
+            cv[j] = nearest_code(fabsf(xv[j]), sm.thr8, sm.bucket8);
         }
         if (full) {
             Codes<VEC>::store(p.mq[sh][cur ^ 1] + e, cm);

@@ -1,6 +1,7 @@
 // adam8_math.cuh -- the arithmetic of the 8-bit Adam step that is not the
 // fp32 Adam update: the two code maps and their nearest-code search, and the
-// exact division by a per-step constant.  Included inside an anonymous
+// exact division by a divisor used many times (a per-step bias correction, a
+// block's scale).  Included inside an anonymous
 // namespace by adam8.cu (and by the test program that checks these functions
 // exhaustively against a plain search and the IEEE division), after <cmath>,
 // <cstring> and <stdint.h>.
@@ -76,7 +77,7 @@ bool build_search(const float* mag, int count, float* thr, uint8_t* bucket) {
 // ----------------------------------------------------------- device helpers ---
 
 // Index of the map value nearest to min(a, 1) for a >= 0, ties to the
-// smaller; a NaN (0 * inf when a scale below 2^-126 has no finite reciprocal)
+// smaller; a NaN (inf / inf, only on a step that overflowed and is dropped)
 // gives 0, as a nearest search does.  Raising a to 2^-26 moves nothing across
 // a threshold (the lowest is 5e-8); with the clamp to 1 it keeps the bucket
 // index inside the table for every input.
@@ -88,20 +89,32 @@ __device__ __forceinline__ uint32_t nearest_code(float a, const float* thr, cons
 
 // VEC one-byte codes per thread: one 8- or 16-byte access.
 template <int VEC> struct Codes;
-// x / d rounded once to nearest, for d = 1 - beta^t (0 < d <= 1, a per-step
-// constant) with y = RN(1 / d) formed once: q = x y, then two corrections
+// x / d rounded once to nearest, for a divisor d used many times (1 - beta^t
+// in a step, a block's scale) with y = RN(1 / d) formed once: q = x y, then two corrections
 // q <- q + (x - d q) y whose residuals the fused multiply-add forms exactly.
 // After the first, q is within one ulp of x / d (a faithful quotient); then
 // its residual is exact and, y being the correctly rounded reciprocal, the
 // second correction yields the correctly rounded quotient (Markstein's
 // theorem; P. Markstein, "Computation of elementary functions on the IBM RISC
 // System/6000 processor", 1990; also Cornea, Harrison and Tang, "Scientific
-// Computing on Itanium-based Systems", 2002).  Valid for x = 0 and for
-// |x| >= 2^-100, where no quotient, product or residual leaves the normal
-// range; the caller sends smaller values to the IEEE division.
+// Computing on Itanium-based Systems", 2002).  For d = 1 - beta^t in (0, 1]:
+// valid for x = 0 and for |x| >= 2^-100, where no quotient, product or
+// residual leaves the normal range; the caller sends smaller values to the
+// IEEE division.  For a block's scale, see scale_divisor_ok.
 __device__ __forceinline__ float div_by_constant(float x, float d, float y) {
     float q = __fmul_rn(x, y);
     q = __fmaf_rn(__fmaf_rn(-q, d, x), y, q);
     return __fmaf_rn(__fmaf_rn(-q, d, x), y, q);
 }
 
+// Whether div_by_constant gives the codes of the IEEE quotient x / d for
+// every |x| <= d when d is a block's largest magnitude (the normalization of
+// m' and v' before their codes are looked up).  For d in [2^-64, 2^64]:
+//   - where x / d >= 2^-27 in magnitude, 1 / d and every quotient, product
+//     and residual of div_by_constant are normal floats (the residual's unit,
+//     ulp(q) ulp(d) >= 2^-137, stays above the subnormal unit), so the result
+//     is the correctly rounded quotient;
+//   - where x / d < 2^-27, both results lie far below the lowest code
+//     threshold (5e-8), so both take code 0.
+// Outside that range the caller divides with __fdiv_rn.
+__device__ __forceinline__ bool scale_divisor_ok(float d) { return d >= 0x1p-64f && d <= 0x1p64f; }
