@@ -285,14 +285,19 @@ ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t
  *     zero_shard_step (without flag_dev);
  *   - n_shards above ZS_NOALLOC_MAX_SHARDS returns ZS_ERR_ARG (the text is in
  *     zero_last_error()) and launches nothing;
- *   - the first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture;
+ *   - the first call on each device (and in each new context of it) looks up
+ *     the array's device address with that device current; make that first
+ *     call before any stream capture;
+ *   - the kernels are those of zero_shard_step, with the same grouping of
+ *     consecutive shards into one launch; each launch ORs its non-finite
+ *     test into the word of its first shard;
  *   - every call shares the array, and it keeps the last call's contents; each
  *     call clears the words it uses before its kernels run.  Calls whose work
  *     overlaps on the GPU (other streams, other host threads) race on it, so
  *     order them.
- * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
- * 2.1, Fact 1 (the entry point itself has no counterpart in the pages). */
+ *   - the array's address is cached per device and per CUDA context (by the
+ *     driver's context ID), so a context created after cudaDeviceReset looks
+ *     it up again. */
 ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                        const zs_adam* hp, double loss_scale, int64_t step,
                                        int32_t cur, void* stream, int32_t* overflow_out);
@@ -306,8 +311,17 @@ ZS_API int32_t zero_ctrl_init(zs_ctrl* ctrl_dev, double loss_scale, void* stream
 /* The same step with no host synchronisation (CUDA-graph friendly): the loss
  * scale, t and the ping-pong set come from *ctrl_dev, and the commit-or-skip
  * decision runs on the device.  Enqueues the fused kernels of every shard
- * with n > 0 (zero_shard_reduce_adam_all_async) and then one commit kernel
- * (zero_step_commit_async).
+ * with n > 0 (as zero_shard_reduce_adam_all_async), then:
+ *   - no shard with a qwZ copy: the last fused launch finishes the step
+ *     itself (its last block to finish commits or skips, as
+ *     zero_step_commit_async decides), and one restore kernel follows that
+ *     rewrites the params from master[cur] only if the step overflowed and
+ *     otherwise ends at once.  These kernels are launched with programmatic
+ *     stream serialization: each may be scheduled while the previous kernel
+ *     in the stream ends, and waits for it before touching memory;
+ *   - otherwise one commit kernel (zero_step_commit_async), which also writes
+ *     the qwZ copies' trailing blocks.
+ * The results are those of the two-call form in either case.
  * Source: "ZeRO Stage 1 Math", "The per-step mechanics", beats 2-3; "DeepSpeed ZeRO Stages", sec.
  * 2.1, Fact 1. */
 ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,

@@ -26,8 +26,12 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <cuda.h>  // driver types only (CUcontext); the entry point is fetched at run time
+
+#include <map>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "zs_internal.h"
 
@@ -38,6 +42,47 @@ constexpr int kCommitThreads = 512;    // threads per block of the commit kernel
 constexpr int kCastThreads = 256;
 
 #include "step_common.cuh"
+
+// ------------------------------------------------------ launch ordering ---
+
+// Programmatic dependent launch (sm_90 and later).  A kernel launched with the
+// programmatic stream-serialization attribute may be scheduled while the
+// kernel before it in the stream is still running; griddep_wait() returns once
+// that kernel has completed and its writes are visible (at once when the
+// launch carried no such dependency), so every kernel that can be launched
+// this way calls it before touching memory.  griddep_launch_dependents() lets
+// the next such kernel of the stream be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// The end of a step in the control block, called by thread 0 of each of the
+// `total` blocks that take part, after that block's overflow atomic: the last
+// block to arrive commits (flip the state set, t += 1, beta^t updated) or, if
+// the step overflowed, skips (L <- max(L / 2, 1), skipped += 1); it records
+// the flag in last_overflow and clears the flag and the arrival count for the
+// next step.  Nothing waits: the other blocks just leave.
+__device__ void arrive_and_finish(zs_ctrl* ctrl, uint32_t total, double beta1, double beta2) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&ctrl->arrivals, 1u);
+    if (prev != total - 1) return;
+    __threadfence();  // every block's flag update is visible past this point
+    volatile zs_ctrl* c = ctrl;
+    const int ovf = c->overflow;
+    c->last_overflow = ovf;
+    if (ovf) {
+        const double half = __dmul_rn(c->loss_scale, 0.5);
+        c->loss_scale = half < 1.0 ? 1.0 : half;
+        c->skipped = c->skipped + 1;
+    } else {
+        c->cur = c->cur ^ 1;
+        c->step = c->step + 1;
+        c->beta1_pow = __dmul_rn(c->beta1_pow, beta1);
+        c->beta2_pow = __dmul_rn(c->beta2_pow, beta2);
+    }
+    c->overflow = 0;
+    c->arrivals = 0u;
+    __threadfence();
+}
 
 // ------------------------------------------------------------ fused kernel ---
 
@@ -57,6 +102,7 @@ struct StepArgs {
     zs_adam hp;           // hyper-parameters for device-resolved coefficients
     const zs_ctrl* ctrl;  // non-null: loss scale, t and cur come from here
     int32_t* flag;        // overflow accumulator (ORed)
+    zs_ctrl* commit;      // non-null: this launch ends the step (arrive_and_finish)
     int8_t* qcodes;       // qwZ copy (QZ kernels only)
     float* qscales;
 };
@@ -99,29 +145,22 @@ __device__ __forceinline__ uint32_t step_elements(const uint16_t* const (&grads)
 // have: +6.8 % on the ragged workload's qwZ step, +24 % at N_d = 8 (measured).
 // With 32 or 64 contributions it already uses 128, and the promise measured
 // 2.8 % slower there, so it is not made.
+//
+// The 16-element kernel with a run-time N_d and no qwZ copy also gets the
+// promise: without it, the end-of-step code after its element loop led the
+// compiler to a 99-register allocation of the loop (127 before that code was
+// added), 24 % slower on the N_d = 8 GPT-2-small shard (0.112 -> 0.139 ms per
+// step, measured); with it the loop gets 128.
 template <int VEC, int ND, bool QZ>
-constexpr int step_min_blocks() { return (VEC == 16 && QZ && ND <= 16) ? 2 : 0; }
+constexpr int step_min_blocks() { return (VEC == 16 && (QZ ? ND <= 16 : ND == 0)) ? 2 : 0; }
+// The grouped kernel keeps the first rule (its registers did not move).
+template <int VEC, int ND, bool QZ>
+constexpr int group_min_blocks() { return (VEC == 16 && QZ && ND <= 16) ? 2 : 0; }
 
+// The element loop of shard_step_kernel over the shard (set cur in, set
+// cur ^ 1 out); returns this thread's non-finite bits.
 template <int CAP, int VEC, int ND, bool QZ, bool FAST>
-__global__ void __launch_bounds__(kThreads, step_min_blocks<VEC, ND, QZ>())
-shard_step_kernel(const __grid_constant__ StepArgs<CAP> p) {
-    __shared__ Coef s_coef;
-    __shared__ int s_cur;
-    if (threadIdx.x == 0) {
-        if (p.ctrl != nullptr) {
-            const zs_ctrl* ctrl = p.ctrl;
-            const double p1 = __dmul_rn(ctrl->beta1_pow, p.hp.beta1);  // beta1^(t+1)
-            const double p2 = __dmul_rn(ctrl->beta2_pow, p.hp.beta2);
-            s_coef = coef_device(p.hp, p1, p2, p.n_d, ctrl->loss_scale);
-            s_cur = ctrl->cur;
-        } else {
-            s_coef = p.coef;
-            s_cur = p.cur;
-        }
-    }
-    __syncthreads();
-    const Coef c = s_coef;
-    const int cur = s_cur;
+__device__ __forceinline__ uint32_t step_range(const StepArgs<CAP>& p, const Coef c, const int cur) {
     const float* th_in = p.master[cur];
     const float* m_in = p.m[cur];
     const float* v_in = p.v[cur];
@@ -172,8 +211,42 @@ shard_step_kernel(const __grid_constant__ StepArgs<CAP> p) {
                                                    m_out, v_out, th);
         }
     }
+    return bad;
+}
+
+template <int CAP, int VEC, int ND, bool QZ, bool FAST>
+__global__ void __launch_bounds__(kThreads, step_min_blocks<VEC, ND, QZ>())
+shard_step_kernel(const __grid_constant__ StepArgs<CAP> p) {
+    __shared__ Coef s_coef;
+    __shared__ int s_cur;
+    griddep_wait();
+    griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        if (p.ctrl != nullptr) {
+            const zs_ctrl* ctrl = p.ctrl;
+            const double p1 = __dmul_rn(ctrl->beta1_pow, p.hp.beta1);  // beta1^(t+1)
+            const double p2 = __dmul_rn(ctrl->beta2_pow, p.hp.beta2);
+            s_coef = coef_device(p.hp, p1, p2, p.n_d, ctrl->loss_scale);
+            s_cur = ctrl->cur;
+        } else {
+            s_coef = p.coef;
+            s_cur = p.cur;
+        }
+    }
+    __syncthreads();
+    const Coef c = s_coef;
+    const int cur = s_cur;
+    const uint32_t bad = step_range<CAP, VEC, ND, QZ, FAST>(p, c, cur);
     // overflow: warp/block OR, one atomic per block that saw a non-finite value
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
+    // (a step with a qwZ copy ends in the commit kernel, so QZ kernels carry no
+    // end-of-step code)
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        if (any_bad) atomicOr(p.flag, 1);
+        if constexpr (!QZ) {
+            if (p.commit != nullptr) arrive_and_finish(p.commit, gridDim.x, p.hp.beta1, p.hp.beta2);
+        }
+    }
 }
 
 // ------------------------------------------------ several shards, one launch ---
@@ -202,6 +275,7 @@ struct GroupArgs {
     zs_adam hp;
     const zs_ctrl* ctrl;  // non-null: loss scale, t and cur come from here
     int32_t* flag;
+    zs_ctrl* commit;      // non-null: this launch ends the step (arrive_and_finish)
 };
 
 // The fused step of several shards in one persistent launch: the grid walks
@@ -216,10 +290,12 @@ struct GroupArgs {
 // lanes that hold one 256-parameter block always belong to one shard and
 // reduce its scale by shuffles, as in shard_step_kernel.
 template <int CAP, int VEC, int ND, bool QZ, bool FAST>
-__global__ void __launch_bounds__(kThreads, step_min_blocks<VEC, ND, QZ>())
+__global__ void __launch_bounds__(kThreads, group_min_blocks<VEC, ND, QZ>())
 group_step_kernel(const __grid_constant__ GroupArgs<CAP> a) {
     __shared__ Coef s_coef;
     __shared__ int s_cur;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         if (a.ctrl != nullptr) {
             const zs_ctrl* ctrl = a.ctrl;
@@ -285,7 +361,13 @@ group_step_kernel(const __grid_constant__ GroupArgs<CAP> a) {
             }
         }
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.flag, 1);
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        if (any_bad) atomicOr(a.flag, 1);
+        if constexpr (!QZ) {
+            if (a.commit != nullptr) arrive_and_finish(a.commit, gridDim.x, a.hp.beta1, a.hp.beta2);
+        }
+    }
 }
 
 // ---------------------------------------------------------- commit kernel ---
@@ -415,30 +497,31 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0) arrive_and_finish(ctrl, gridDim.x, p.beta1, p.beta2);
+}
+
+// After a step whose last fused launch already finished it in the control
+// block (arrive_and_finish): if that step overflowed, re-cast each shard's
+// fp16 slice from the kept master weights (set cur, unchanged by a skip);
+// otherwise every block leaves at once.  Shards with a qwZ copy do not take
+// this path.  Launched with programmatic serialization, so its launch overlaps
+// the end of the fused kernel; it reads the control block only after that
+// kernel has completed.
+template <int MAXS>
+__global__ void __launch_bounds__(kCommitThreads) restore_kernel(const __grid_constant__ CommitArgs<MAXS> p) {
+    __shared__ int s_ovf, s_cur;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned prev = atomicAdd(&ctrl->arrivals, 1u);
-        if (prev == gridDim.x - 1) {
-            // every block has read overflow and cur: finish the step
-            __threadfence();
-            volatile zs_ctrl* c = ctrl;
-            const int ovf = c->overflow;
-            c->last_overflow = ovf;
-            if (ovf) {
-                const double half = __dmul_rn(c->loss_scale, 0.5);
-                c->loss_scale = half < 1.0 ? 1.0 : half;
-                c->skipped = c->skipped + 1;
-            } else {
-                c->cur = c->cur ^ 1;
-                c->step = c->step + 1;
-                c->beta1_pow = __dmul_rn(c->beta1_pow, p.beta1);
-                c->beta2_pow = __dmul_rn(c->beta2_pow, p.beta2);
-            }
-            c->overflow = 0;
-            c->arrivals = 0u;
-            __threadfence();
-        }
+        s_ovf = *reinterpret_cast<volatile int32_t*>(&p.ctrl->last_overflow);
+        s_cur = *reinterpret_cast<volatile int32_t*>(&p.ctrl->cur);
     }
+    __syncthreads();
+    if (!s_ovf) return;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int s = 0; s < p.n_shards; ++s)
+        cast_range(p.shards[s].master[s_cur], p.shards[s].params, p.shards[s].n, tid, stride);
 }
 
 // qwZ blocks [b0, b1) on their own (see qwz_blocks).
@@ -669,12 +752,39 @@ using zs::valid_hp;
 
 namespace {
 
+// How the fused launches of one step are enqueued.
+struct LaunchOpts {
+    zs_ctrl* commit = nullptr;  // non-null: the step's last launch finishes it in the control block
+    bool pdl = false;           // launch with programmatic stream serialization
+};
+
+// Enqueues kernel<<<blocks, threads, 0, stream>>>(args), with the
+// programmatic-serialization attribute when pdl (the kernel then waits for
+// its predecessor with griddep_wait before touching memory).
+template <typename Args>
+int32_t launch_kernel(void (*kernel)(Args), int blocks, int threads, bool pdl, cudaStream_t stream,
+                      const Args& args, const char* name) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args);
+    if (err != cudaSuccess) return zs::cuda_fail(err, name);
+    return zs::check_launch(name);
+}
+
 template <int CAP, int VEC, int ND, bool QZ, bool FAST = false>
-int32_t launch_step_vec(const StepArgs<CAP>& a, cudaStream_t stream) {
+int32_t launch_step_vec(const StepArgs<CAP>& a, bool pdl, cudaStream_t stream) {
     const void* k = (const void*)shard_step_kernel<CAP, VEC, ND, QZ, FAST>;
     const int blocks = persistent_blocks(k, kThreads, a.n / VEC > 0 ? a.n / VEC : 1);
-    shard_step_kernel<CAP, VEC, ND, QZ, FAST><<<blocks, kThreads, 0, stream>>>(a);
-    return zs::check_launch("shard_step_kernel");
+    return launch_kernel(shard_step_kernel<CAP, VEC, ND, QZ, FAST>, blocks, kThreads, pdl, stream, a,
+                         "shard_step_kernel");
 }
 
 // ZS_MATH_FAST runs the FAST instantiation where it measured faster: the
@@ -682,18 +792,19 @@ int32_t launch_step_vec(const StepArgs<CAP>& a, cudaStream_t stream) {
 // compiled for N_d = 16, 32, 64 (+1.3 % at 16), without a qwZ copy (with one,
 // the 8-element kernel measured no gain: 172.4 vs 173.4 Gparams/s at N_d = 4).
 template <int CAP, int VEC, int ND, bool QZ>
-int32_t launch_math(const StepArgs<CAP>& a, bool fast, cudaStream_t stream) {
+int32_t launch_math(const StepArgs<CAP>& a, bool fast, bool pdl, cudaStream_t stream) {
     if constexpr (!QZ && (VEC == 8 || (VEC == 16 && ND > 0))) {
-        if (fast) return launch_step_vec<CAP, VEC, ND, QZ, true>(a, stream);
+        if (fast) return launch_step_vec<CAP, VEC, ND, QZ, true>(a, pdl, stream);
     }
-    return launch_step_vec<CAP, VEC, ND, QZ>(a, stream);
+    return launch_step_vec<CAP, VEC, ND, QZ>(a, pdl, stream);
 }
 
 // CAP sizes the contribution table; ND > 0 compiles the kernel for exactly ND
 // contributions (CAP == ND), ND == 0 reads n_d at run time.
 template <int CAP, int ND>
 int32_t launch_step_cap(const zs_shard& s, int32_t n_d, int width, const Coef* coef, int32_t cur,
-                        const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
+                        const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, const LaunchOpts& o,
+                        cudaStream_t stream) {
     StepArgs<CAP> a;
     for (int k = 0; k < CAP; ++k) a.grads[k] = k < n_d ? s.grads[k] : nullptr;
     for (int i = 0; i < 2; ++i) {
@@ -709,47 +820,53 @@ int32_t launch_step_cap(const zs_shard& s, int32_t n_d, int width, const Coef* c
     a.hp = hp;
     a.ctrl = ctrl;
     a.flag = flag;
+    a.commit = o.commit;
     a.qcodes = s.qcodes;
     a.qscales = s.qscales;
     const bool qz = s.qcodes != nullptr;
     const bool fast = hp.math == ZS_MATH_FAST;
+    const bool pdl = o.pdl;
     // the wide layout only pays once N_d > 4 (measured); scalar if misaligned
     if constexpr (ND == 0 || ND > 4) {
         if (width == 2 && n_d > 4)
-            return qz ? launch_math<CAP, 16, ND, true>(a, fast, stream) : launch_math<CAP, 16, ND, false>(a, fast, stream);
+            return qz ? launch_math<CAP, 16, ND, true>(a, fast, pdl, stream)
+                      : launch_math<CAP, 16, ND, false>(a, fast, pdl, stream);
     }
     if (width >= 1)
-        return qz ? launch_math<CAP, 8, ND, true>(a, fast, stream) : launch_math<CAP, 8, ND, false>(a, fast, stream);
+        return qz ? launch_math<CAP, 8, ND, true>(a, fast, pdl, stream)
+                  : launch_math<CAP, 8, ND, false>(a, fast, pdl, stream);
     // scalar kernel: the qwZ copy of every block follows in its own pass
-    int32_t rc = launch_step_vec<CAP, 1, ND, false>(a, stream);
+    int32_t rc = launch_step_vec<CAP, 1, ND, false>(a, pdl, stream);
     if (rc == ZS_OK && qz)
         rc = launch_qwz(nullptr, s.params, s.n, s.qcodes, s.qscales, 0, (s.n + kQwzBlock - 1) / kQwzBlock, stream);
     return rc;
 }
 
 int32_t launch_step(const zs_shard& s, int32_t n_d, int width, const Coef* coef, int32_t cur,
-                    const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
+                    const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, const LaunchOpts& o,
+                    cudaStream_t stream) {
     // A kernel compiled for the exact count pays for 16 or more contributions
     // (measured: +3.4% at N_d = 16, +0.5% at N_d = 64).  For N_d <= 8 the
     // straight-line version issued every contribution load at once and ran
     // 4-7% slower than the run-time loop, so small counts use the latter.
     switch (n_d) {
-    case 16: return launch_step_cap<16, 16>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    case 32: return launch_step_cap<32, 32>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    case 64: return launch_step_cap<64, 64>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
+    case 16: return launch_step_cap<16, 16>(s, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    case 32: return launch_step_cap<32, 32>(s, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    case 64: return launch_step_cap<64, 64>(s, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
     default: break;
     }
-    if (n_d <= 4) return launch_step_cap<4, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    if (n_d <= 16) return launch_step_cap<16, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    if (n_d <= 64) return launch_step_cap<64, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    return launch_step_cap<ZS_MAX_ND, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, stream);
+    if (n_d <= 4) return launch_step_cap<4, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    if (n_d <= 16) return launch_step_cap<16, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    if (n_d <= 64) return launch_step_cap<64, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    return launch_step_cap<ZS_MAX_ND, 0>(s, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
 }
 
 // One launch of the grouped kernel over shards[0, count), all with access
 // width `width` (1 or 2) and no qwZ copy.
 template <int CAP, int ND>
 int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int width, const Coef* coef, int32_t cur,
-                         const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
+                         const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, const LaunchOpts& o,
+                         cudaStream_t stream) {
     GroupArgs<CAP> a;
     const int vec = (width == 2 && n_d > 4) ? 16 : 8;
     const bool qz = shards[0].qcodes != nullptr;   // all or none of the group
@@ -780,11 +897,11 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
     a.hp = hp;
     a.ctrl = ctrl;
     a.flag = flag;
+    a.commit = o.commit;
     const bool fast = hp.math == ZS_MATH_FAST;
     auto go = [&](auto kernel) {
         const int blocks = persistent_blocks((const void*)kernel, kThreads, a.vstart[count] > 0 ? a.vstart[count] : 1);
-        kernel<<<blocks, kThreads, 0, stream>>>(a);
-        return zs::check_launch("group_step_kernel");
+        return launch_kernel(kernel, blocks, kThreads, o.pdl, stream, a, "group_step_kernel");
     };
     // the same kernel choice as for one shard (launch_step_cap / launch_math)
     if constexpr (ND == 0 || ND > 4) {
@@ -802,43 +919,94 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
 }
 
 int32_t launch_group(const zs_shard* shards, int count, int32_t n_d, int width, const Coef* coef, int32_t cur,
-                     const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
+                     const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, const LaunchOpts& o,
+                     cudaStream_t stream) {
     switch (n_d) {
-    case 16: return launch_group_cap<16, 16>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    case 32: return launch_group_cap<32, 32>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    case 64: return launch_group_cap<64, 64>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, stream);
+    case 16: return launch_group_cap<16, 16>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    case 32: return launch_group_cap<32, 32>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    case 64: return launch_group_cap<64, 64>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
     default: break;
     }
-    if (n_d <= 4) return launch_group_cap<4, 0>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    if (n_d <= 16) return launch_group_cap<16, 0>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, stream);
-    return launch_group_cap<64, 0>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, stream);
+    if (n_d <= 4) return launch_group_cap<4, 0>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    if (n_d <= 16) return launch_group_cap<16, 0>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
+    return launch_group_cap<64, 0>(shards, count, n_d, width, coef, cur, hp, ctrl, flag, o, stream);
 }
 
-// The fused kernels of one step for shards[0, n_shards): consecutive
-// non-empty shards with the same vector width, all with or all without a qwZ
-// copy, go up to kGroupMax per launch of the grouped kernel (n_d <= 64);
-// every other shard gets its own launch.  Empty shards launch nothing.
-int32_t launch_steps(const zs_shard* shards, int32_t n_shards, int32_t n_d, const int* width, const Coef* coef,
-                     int32_t cur, const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, cudaStream_t stream) {
-    int32_t i = 0;
+// The fused launches of one step for shards[0, n_shards), in order: runs of
+// consecutive non-empty shards with the same vector width, all with or all
+// without a qwZ copy, go up to kGroupMax per launch of the grouped kernel
+// (n_d <= 64); every other shard gets its own launch; empty shards launch
+// nothing.  plan[k] = {first shard, shard count}; returns the launch count.
+struct LaunchRange {
+    int32_t first, count;
+};
+int32_t plan_steps(const zs_shard* shards, int32_t n_shards, int32_t n_d, const int* width, LaunchRange* plan) {
+    int32_t np = 0, i = 0;
     while (i < n_shards) {
-        const zs_shard& s = shards[i];
-        if (s.n == 0) { ++i; continue; }
+        if (shards[i].n == 0) { ++i; continue; }
         const bool groupable = n_d <= 64 && width[i] >= 1;
-        const bool qz = s.qcodes != nullptr;
+        const bool qz = shards[i].qcodes != nullptr;
         int32_t j = i + 1;
         if (groupable) {
             while (j < n_shards && j - i < kGroupMax && width[j] == width[i] && (shards[j].qcodes != nullptr) == qz &&
                    shards[j].n > 0)
                 ++j;
         }
-        int32_t rc;
-        if (groupable && j - i > 1) rc = launch_group(shards + i, j - i, n_d, width[i], coef, cur, hp, ctrl, flag, stream);
-        else rc = launch_step(s, n_d, width[i], coef, cur, hp, ctrl, flag, stream);
-        if (rc != ZS_OK) return rc;
-        i = groupable ? j : i + 1;
+        plan[np++] = LaunchRange{i, j - i};
+        i = j;
     }
+    return np;
+}
+
+// Enqueues the fused launches of one step (see plan_steps).  flag: the
+// step's overflow word; with flag_per_launch, launch k writes flag[first
+// shard of launch k] instead.  o.commit is given to the last launch only;
+// *committed says whether a launch took it (false when nothing launched).
+int32_t launch_steps(const zs_shard* shards, int32_t n_shards, int32_t n_d, const int* width, const Coef* coef,
+                     int32_t cur, const zs_adam& hp, const zs_ctrl* ctrl, int32_t* flag, bool flag_per_launch,
+                     const LaunchOpts& o, bool* committed, cudaStream_t stream) {
+    LaunchRange plan[ZS_MAX_SHARDS];
+    const int32_t np = plan_steps(shards, n_shards, n_d, width, plan);
+    if (committed) *committed = false;
+    for (int32_t k = 0; k < np; ++k) {
+        LaunchOpts ok = o;
+        if (k + 1 < np) ok.commit = nullptr;
+        const LaunchRange& L = plan[k];
+        int32_t* f = flag_per_launch ? flag + L.first : flag;
+        const int32_t rc = L.count > 1
+            ? launch_group(shards + L.first, L.count, n_d, width[L.first], coef, cur, hp, ctrl, f, ok, stream)
+            : launch_step(shards[L.first], n_d, width[L.first], coef, cur, hp, ctrl, f, ok, stream);
+        if (rc != ZS_OK) return rc;
+    }
+    if (committed) *committed = o.commit != nullptr && np > 0;
     return ZS_OK;
+}
+
+// The restore pass after a step that a fused launch finished (restore_kernel),
+// with programmatic serialization.
+template <int MAXS>
+int32_t launch_restore_cap(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream) {
+    CommitArgs<MAXS> a;
+    for (int i = 0; i < MAXS; ++i) {
+        if (i < n_shards)
+            a.shards[i] = CommitShard{shards[i].params, {shards[i].master[0], shards[i].master[1]}, shards[i].n,
+                                      nullptr, nullptr};
+        else
+            a.shards[i] = CommitShard{nullptr, {nullptr, nullptr}, 0, nullptr, nullptr};
+    }
+    a.n_shards = n_shards;
+    a.beta1 = 0.0;
+    a.beta2 = 0.0;
+    a.ctrl = ctrl;
+    // one block per SM, as the commit kernel: full bandwidth for the restore
+    return launch_kernel(restore_kernel<MAXS>, zs::device_sm_count(), kCommitThreads, true, stream, a,
+                         "restore_kernel");
+}
+
+int32_t launch_restore(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream) {
+    if (n_shards <= 1) return launch_restore_cap<1>(shards, n_shards, ctrl, stream);
+    if (n_shards <= 16) return launch_restore_cap<16>(shards, n_shards, ctrl, stream);
+    return launch_restore_cap<ZS_MAX_SHARDS>(shards, n_shards, ctrl, stream);
 }
 
 }  // namespace
@@ -871,7 +1039,8 @@ ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t err = cudaMemsetAsync(flag_dev, 0, sizeof(int32_t), st);
     if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step: clear flag");
-    rc = launch_steps(shards, n_shards, n_d, width, &coef, cur, *hp, nullptr, flag_dev, st);
+    rc = launch_steps(shards, n_shards, n_d, width, &coef, cur, *hp, nullptr, flag_dev, false, LaunchOpts{}, nullptr,
+                      st);
     if (rc != ZS_OK) return rc;
     int32_t flag = 0;
     err = cudaMemcpyAsync(&flag, flag_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
@@ -894,11 +1063,40 @@ ZS_API int32_t zero_shard_step(const zs_shard* shards, int32_t n_shards, int32_t
 // noalloc_scratch() looks up the device address.
 static __device__ __align__(256) int32_t g_noalloc_scratch[ZS_NOALLOC_MAX_SHARDS];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// Device address of g_noalloc_scratch for the current device and context,
+// looked up once per (device, context) pair, with that device current, and
+// cached.  The context is identified by the driver's context ID, unique for
+// the life of the process, so a context made after cudaDeviceReset (which
+// reloads the library's module, possibly at another address) gets its own
+// lookup instead of a stale pointer, even if its handle repeats.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The calling thread's current context ID (0 if there is no current context
+// or the driver cannot say).
+static unsigned long long current_context_id() {
+    static const std::pair<CtxGetCurrentFn, CtxGetIdFn> fns = [] {
+        void* get = nullptr;
+        void* id = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        const cudaError_t e1 = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &get, 12000, cudaEnableDefault, &q1);
+        const cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuCtxGetId", &id, 12000, cudaEnableDefault, &q2);
+        if (e1 != cudaSuccess || e2 != cudaSuccess) cudaGetLastError();  // a failed query leaves nothing behind
+        if (e1 != cudaSuccess || q1 != cudaDriverEntryPointSuccess) get = nullptr;
+        if (e2 != cudaSuccess || q2 != cudaDriverEntryPointSuccess) id = nullptr;
+        return std::make_pair(reinterpret_cast<CtxGetCurrentFn>(get), reinterpret_cast<CtxGetIdFn>(id));
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (fns.first == nullptr || fns.second == nullptr || fns.first(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        fns.second(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 static int32_t* noalloc_scratch(int32_t* status) {
     static std::mutex mu;
-    static std::unordered_map<int, int32_t*> by_device;
+    static std::map<std::pair<int, unsigned long long>, int32_t*> cache;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) {
@@ -906,8 +1104,13 @@ static int32_t* noalloc_scratch(int32_t* status) {
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
-    auto it = by_device.find(dev);
-    if (it != by_device.end()) return it->second;
+    const unsigned long long id = current_context_id();
+    if (id != 0) {
+        auto it = cache.find(std::make_pair(dev, id));
+        if (it != cache.end()) return it->second;
+    }
+    // first call in this context (the lookup also makes the device's context
+    // current if no CUDA call has yet)
     void* addr = nullptr;
     err = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
     if (err != cudaSuccess || addr == nullptr) {
@@ -915,8 +1118,9 @@ static int32_t* noalloc_scratch(int32_t* status) {
                                 "zero_shard_step_noalloc: cudaGetSymbolAddress");
         return nullptr;
     }
-    by_device[dev] = static_cast<int32_t*>(addr);
-    return by_device[dev];
+    const unsigned long long id_now = current_context_id();
+    if (id_now != 0) cache[std::make_pair(dev, id_now)] = static_cast<int32_t*>(addr);
+    return static_cast<int32_t*>(addr);
 }
 
 ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards, int32_t n_d,
@@ -945,11 +1149,11 @@ ZS_API int32_t zero_shard_step_noalloc(const zs_shard* shards, int32_t n_shards,
     // the array keeps the previous call's words: clear the ones this call uses
     cudaError_t err = cudaMemsetAsync(scratch, 0, sizeof(int32_t) * n_shards, st);
     if (err != cudaSuccess) return zs::cuda_fail(err, "zero_shard_step_noalloc: clear scratch");
-    for (int32_t i = 0; i < n_shards; ++i) {
-        if (shards[i].n == 0) continue;
-        rc = launch_step(shards[i], n_d, width[i], &coef, cur, *hp, nullptr, scratch + i, st);
-        if (rc != ZS_OK) return rc;
-    }
+    // the launches of zero_shard_step (grouped where the shards allow); each
+    // launch ORs into the word of its first shard
+    rc = launch_steps(shards, n_shards, n_d, width, &coef, cur, *hp, nullptr, scratch, true, LaunchOpts{}, nullptr,
+                      st);
+    if (rc != ZS_OK) return rc;
     int32_t words[ZS_NOALLOC_MAX_SHARDS];
     err = cudaMemcpyAsync(words, scratch, sizeof(int32_t) * n_shards, cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
@@ -980,7 +1184,7 @@ ZS_API int32_t zero_shard_reduce_adam_async(const zs_shard* shard, int32_t n_d, 
     int32_t rc = check_shard(*shard, n_d, &width);
     if (rc != ZS_OK) return rc;
     if (shard->n == 0) return ZS_OK;
-    return launch_step(*shard, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow,
+    return launch_step(*shard, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, LaunchOpts{},
                        (cudaStream_t)stream);
 }
 
@@ -1008,8 +1212,20 @@ ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, i
     int32_t rc = check_shard_list(shards, n_shards, n_d, width);
     if (rc != ZS_OK) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    rc = launch_steps(shards, n_shards, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, st);
+    // Without a qwZ copy the step's last fused launch finishes the step in the
+    // control block itself and a restore pass follows (it leaves at once unless
+    // the step overflowed), both with programmatic serialization; with one,
+    // the commit kernel also writes the qwZ copies' trailing blocks.
+    bool any_qwz = false;
+    for (int32_t i = 0; i < n_shards; ++i) any_qwz |= shards[i].qcodes != nullptr;
+    LaunchOpts o;
+    o.commit = any_qwz ? nullptr : ctrl_dev;
+    o.pdl = !any_qwz;
+    bool committed = false;
+    rc = launch_steps(shards, n_shards, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, false, o,
+                      &committed, st);
     if (rc != ZS_OK) return rc;
+    if (committed) return launch_restore(shards, n_shards, ctrl_dev, st);
     return launch_commit(shards, n_shards, *hp, ctrl_dev, st);
 }
 
@@ -1020,8 +1236,8 @@ ZS_API int32_t zero_shard_reduce_adam_all_async(const zs_shard* shards, int32_t 
     int width[ZS_MAX_SHARDS];
     int32_t rc = check_shard_list(shards, n_shards, n_d, width);
     if (rc != ZS_OK) return rc;
-    return launch_steps(shards, n_shards, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow,
-                        (cudaStream_t)stream);
+    return launch_steps(shards, n_shards, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, false,
+                        LaunchOpts{}, nullptr, (cudaStream_t)stream);
 }
 
 // Device-usable address of page-locked, mapped host memory (nullptr if the
@@ -1067,7 +1283,7 @@ ZS_API int32_t zero_shard_step_host(const zs_shard* shard, int32_t n_d, const zs
     }
     cudaStream_t st = (cudaStream_t)stream;
     if (dev.n > 0) {
-        rc = launch_step(dev, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, st);
+        rc = launch_step(dev, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, LaunchOpts{}, st);
         if (rc != ZS_OK) return rc;
     }
     rc = launch_commit(&dev, 1, *hp, ctrl_dev, st);
