@@ -4,11 +4,12 @@ already reserved the device, where a cudaMalloc of its own would bypass that
 pool or fail).  It keeps its overflow words in an array compiled into the
 library instead of a caller buffer.
 
-Checked here through the C ABI against the existing zero_shard_step on the
-same inputs, on several calls in a row (a normal step, an overflow step, then
-a normal step again, which also shows the shared array is cleared between
-calls), within the parity tolerances of the other tests.  This file is named
-to be collected last, and it needs nothing from the other tests.
+Checked here through the C ABI, on several calls in a row (a normal step, an
+overflow step, then a normal step again, which also shows the shared array is
+cleared between calls), against both the existing zero_shard_step on the same
+inputs and the oracle, within the parity tolerances of the other tests.  The
+three shards of a call share one grouped launch, as in zero_shard_step.  This
+file is named to be collected last, and it needs nothing from the other tests.
 """
 import ctypes
 
@@ -17,7 +18,7 @@ import pytest
 import torch
 
 from zero_partitioned_mixed_partition_gb300 import synth
-from parity_util import assert_f16_close, assert_f32_close, f16_bits, to_np
+from parity_util import OracleShard, assert_f16_close, assert_f32_close, f16_bits, oracle_group_step, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -37,30 +38,41 @@ def _shards(zs, dev, sizes, n_d, seed):
     return views, keep
 
 
-def test_noalloc_matches_zero_shard_step(zs, cuda_device):
+class _Hp:
+    """The hyper-parameters in the form the oracle helpers read."""
+    lr, beta1, beta2, eps, weight_decay = 1e-3, 0.9, 0.999, 1e-8, 0.01
+
+
+def test_noalloc_matches_zero_shard_step_and_oracle(zs, oracle, cuda_device):
     sizes, n_d, loss_scale = [4099, 2048 * 6 + 3, 17], 4, 256.0
-    hp = zs.adam(1e-3, weight_decay=0.01)
+    hp = zs.adam(_Hp.lr, _Hp.beta1, _Hp.beta2, _Hp.eps, _Hp.weight_decay)
     ref_views, ref_keep = _shards(zs, cuda_device, sizes, n_d, seed=5)
     new_views, new_keep = _shards(zs, cuda_device, sizes, n_d, seed=5)
+    orc = [OracleShard(oracle, to_np(keep[1][0])) for keep in new_keep]
     flag = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    cur, step = 0, 1
+    cur, step, ls, applied = 0, 1, loss_scale, 0
     for call, inject in enumerate([False, True, False]):
         if inject:
             for keep in (ref_keep, new_keep):
                 keep[1][0][2][sizes[1] - 2] = float("inf")    # shard 1, rank 2, a tail element
+        host = [[synth.fp16_bits(g) for g in keep[0]] for keep in new_keep]
         a = zs.zero_shard_step(ref_views, n_d, hp, loss_scale, step, cur, flag)
         b = zs.zero_shard_step_noalloc(new_views, n_d, hp, loss_scale, step, cur)
-        assert a == b == int(inject), (call, a, b)
+        ovf, ls, applied = oracle_group_step(oracle, orc, host, _Hp, ls, applied)
+        assert a == b == ovf == int(inject), (call, a, b, ovf)
         if inject:
             for keep in (ref_keep, new_keep):
                 keep[1][0][2][sizes[1] - 2] = 0.0
             loss_scale = max(loss_scale / 2, 1.0)
         else:
             cur, step = cur ^ 1, step + 1
-        for (_, rm, rmm, rv, rp), (_, nm, nmm, nv, np_) in zip(ref_keep, new_keep):
+        assert (ls, applied) == (loss_scale, step - 1)
+        for i, ((_, rm, rmm, rv, rp), (_, nm, nmm, nv, np_)) in enumerate(zip(ref_keep, new_keep)):
             for x, y, nm_ in ((rm, nm, "master"), (rmm, nmm, "m"), (rv, nv, "v")):
                 assert_f32_close(to_np(y[cur]), to_np(x[cur]), f"call {call} {nm_}")
             assert_f16_close(f16_bits(np_), f16_bits(rp), f"call {call} params")
+            orc[i].compare(to_np(nm[cur]), to_np(nmm[cur]), to_np(nv[cur]), f16_bits(np_),
+                           f"call {call} shard {i} vs oracle")
 
 
 def test_noalloc_refuses_too_many_shards(zs, cuda_device):
