@@ -3,9 +3,13 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload xl] [--impl gb300|reference]
 
 One step = one pass of the whole hot path over one batch of synthetic inputs
-already resident in HBM: the partition/indexing kernel, the fused
-reduce + overflow test + Adam + fp16 cast kernel over the rank's shard, and the
-device-side commit.  Prints ONE JSON line on rank 0.
+already resident in HBM: the fused reduce + overflow test + Adam + fp16 cast
+kernel over the rank's shard, whose last block commits the step on the device,
+and the restore check that rewrites the fp16 slice only after an overflow.
+The partition / indexing kernel runs once per job before the steps and is
+timed on its own.  After the main workload the other target configurations
+(7.5B / N_d = 64 and GPT-2-small by default) are timed the same way and
+reported under "configs".  Prints ONE JSON line on rank 0.
 
 N > 1 (launched by torch.distributed.run): every GPU runs an independent
 replica on its own shard (weak scaling, no collective on the data path); the
@@ -68,6 +72,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--extra-configs", default="7b5,gpt2s",
+                    help="other workloads timed in the same run after the main one (fp32 Adam step only), "
+                         "reported under 'configs'; '' for none")
     return ap.parse_args()
 
 
@@ -373,6 +380,149 @@ def reference_arm(args, rank: int):
 
 # --------------------------------------------------------------- gpu side ---
 
+def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
+    """Pre-warm, warm up and time ``steps`` steps of ``run`` on ``stream``.
+
+    One step is the whole hot path over the stepped shards: the fused
+    reduce + overflow test + Adam + fp16 cast launches and the end of the step
+    (for the fp32 Adam step, the last fused launch commits and a restore
+    kernel follows that leaves at once unless the step overflowed; the other
+    kinds end with the commit kernel).  Returns a dict of the measurements."""
+    import torch
+    import torch.distributed as dist
+    from zero_partitioned_mixed_partition_gb300 import binding
+    from zero_partitioned_mixed_partition_gb300 import dist as zdist
+
+    clip = args.clip > 0
+    sgd_hp = binding.sgd(w.lr, 0.9, w.weight_decay)
+
+    def one_step(ev=None):
+        if clip:
+            with torch.cuda.stream(stream):
+                run.sqnorm.zero_()
+        if ev is not None:
+            ev[0].record(stream)
+        if args.optimizer == "sgd":
+            run.step_sgd(sgd_hp)      # fused kernel(s) and the commit
+        elif args.optimizer == "adam8":
+            run.step_adam8()          # fused kernel(s) and the commit
+        elif not clip:
+            run.step()                # fused kernel(s) ending the step, then the restore check
+        else:
+            binding.zero_shard_grad_sqnorm_all_async(run.views, w.n_d, run.sqnorm, run.ctrl,
+                                                     g_dev=run.gbuf if run.gbuf else None, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+            binding.zero_shard_clipped_adam_all_async(run.views, w.n_d, run.hp, args.clip, run.sqnorm, run.ctrl,
+                                                      g_dev=run.gbuf if run.gbuf else None, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if clip:
+            run.commit()
+
+    # untimed pre-warm: the first seconds of sustained HBM traffic after idle
+    # run a few percent slower; the timed region should see the steady state
+    t0 = time.perf_counter()
+    prewarm_steps = 0
+    while time.perf_counter() - t0 < prewarm_s:
+        for _ in range(10):
+            one_step()
+        prewarm_steps += 10
+        torch.cuda.synchronize()
+    for _ in range(warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    pairs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = binding.zero_kernel_launches()
+    t_start.record(stream)
+    for k in range(steps):
+        one_step(pairs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = binding.zero_kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    out = {"ms_total": ms_total, "kern_ms": [ev[0].elapsed_time(ev[1]) for ev in pairs],
+           "launches": launches, "clocks": clocks, "prewarm_steps": prewarm_steps}
+    if clip:
+        out["norm_ms"] = [ev[0].elapsed_time(ev[2]) for ev in pairs]
+        out["upd_ms"] = [ev[2].elapsed_time(ev[1]) for ev in pairs]
+    ctrl = run.ctrl_host()
+    assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + warmup + steps, ctrl
+    out["ctrl"] = ctrl
+    out["ms_max"] = zdist.max_over_ranks(ms_total, device=torch.device("cuda", local))
+    return out
+
+
+def time_partition(w, dev, stream, repeats: int = 5):
+    """The partition / indexing kernel (zero_partition_layout_device), which
+    runs once per job: its outputs checked against the library's host layout
+    and its launch timed with CUDA events (best of a few, after one untimed
+    run).  Returns (kernel microseconds, fragments)."""
+    import torch
+    from zero_partitioned_mixed_partition_gb300 import binding
+    with torch.cuda.stream(stream):
+        numels_dev = torch.tensor(list(w.numels), dtype=torch.int64, device=dev)
+        scalars = torch.zeros(5, dtype=torch.int64, device=dev)
+        toff = torch.zeros(len(w.numels), dtype=torch.int64, device=dev)
+        soff = torch.zeros(w.n_d + 1, dtype=torch.int64, device=dev)
+        cap = len(w.numels) + w.n_d
+        frags = torch.zeros(cap * 4, dtype=torch.int64, device=dev)
+    best = None
+    for i in range(repeats + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.zero_partition_layout_device(numels_dev, w.n_d, w.align, scalars, toff, soff, frags, cap,
+                                             stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i > 0:
+            us = a.elapsed_time(b) * 1e3
+            best = us if best is None else min(best, us)
+    host = binding.zero_partition_layout(w.numels, w.n_d, w.align)
+    got = scalars.cpu().tolist()
+    assert got[4] == 0 and got[2] == int(host["shard_numel"]), (got, host["shard_numel"])
+    return best, int(got[3])
+
+
+def workload_summary(args, w, run, res, peak, peak_kind):
+    """Rate, bandwidth and roofline of one timed workload."""
+    elems = run.elements_per_step()
+    world = res.get("world", 1)
+    steps = len(res["kern_ms"])
+    bytes_step = run.bytes_per_step()
+    value = elems * world * steps / (res["ms_max"] / 1e3) / 1e9
+    hbm_gbs = bytes_step * world * steps / (res["ms_max"] / 1e3) / 1e9
+    mean_kern_ms = statistics.mean(res["kern_ms"])
+    achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
+    traffic = None
+    per = recorded_traffic("adam")
+    if per and w.n_d in per:
+        traffic = round(per[w.n_d] * elems)
+    return {"workload": workload_label(w, elems), "n_d": w.n_d, "shard_params": elems,
+            "value": round(value, 3), "unit": "Gparams/s", "steps": steps,
+            "ms_per_step": round(res["ms_max"] / steps, 5), "bytes_per_step": bytes_step,
+            "hbm_gbs": round(hbm_gbs, 1), "pct_of_nominal_8tbs": round(100 * hbm_gbs / NOMINAL_HBM_GBS, 2),
+            f"pct_of_{peak_kind}_peak": round(100 * hbm_gbs / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": ("group_step_kernel" if len(run.views) > 1 else "shard_step_kernel")
+                         + " + restore_kernel", "peak_kind": peak_kind,
+                         "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_min": round(min(res["kern_ms"]), 5)},
+            "clocks": res["clocks"], "gpu_launches": int(res["launches"]),
+            "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
+            if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number"}
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -391,7 +541,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    from zero_partitioned_mixed_partition_gb300 import binding, build
+    from zero_partitioned_mixed_partition_gb300 import binding, build, synth
     from zero_partitioned_mixed_partition_gb300 import dist as zdist
     from zero_partitioned_mixed_partition_gb300.runner import WorkloadRunner
 
@@ -401,23 +551,22 @@ def main():
         dist.barrier()
     binding.lib()
 
+    def make_runner(w, stream):
+        if w.rank is not None and world > 1:
+            w = dataclasses.replace(w, rank=zdist.replica_shard(w.rank, rank, w.n_d))
+        with torch.cuda.stream(stream):
+            run = WorkloadRunner(w, dev, stream=stream,
+                                 math=binding.ZS_MATH_FAST if args.math == "fast" else binding.ZS_MATH_IEEE)
+        torch.cuda.synchronize()
+        return w, run
+
     w = workload(args)
-    if w.rank is not None and world > 1:
-        w = dataclasses.replace(w, rank=zdist.replica_shard(w.rank, rank, w.n_d))
     stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        run = WorkloadRunner(w, dev, stream=stream,
-                             math=binding.ZS_MATH_FAST if args.math == "fast" else binding.ZS_MATH_IEEE)
-        numels_dev = torch.tensor(list(w.numels), dtype=torch.int64, device=dev)
-        lay_scalars = torch.zeros(5, dtype=torch.int64, device=dev)
-        lay_toff = torch.zeros(len(w.numels), dtype=torch.int64, device=dev)
-        lay_soff = torch.zeros(w.n_d + 1, dtype=torch.int64, device=dev)
-        cap = len(w.numels) + w.n_d
-        lay_frags = torch.zeros(cap * 4, dtype=torch.int64, device=dev)
-    torch.cuda.synchronize()
+    w, run = make_runner(w, stream)
+    # the partition runs once per job, before the steps: timed on its own
+    part_us, part_frags = time_partition(w, dev, stream)
 
     clip = args.clip > 0
-    sgd_hp = binding.sgd(w.lr, 0.9, w.weight_decay)
     if args.optimizer != "adam" and (clip or args.qwz):
         raise SystemExit(f"--optimizer {args.optimizer} goes without --clip / --qwz")
     if args.optimizer == "adam8":
@@ -427,81 +576,9 @@ def main():
     if args.qwz:
         run.enable_qwz()
 
-    def one_step(ev=None):
-        binding.zero_partition_layout_device(numels_dev, w.n_d, w.align, lay_scalars, lay_toff, lay_soff,
-                                             lay_frags, cap, stream=stream)
-        if args.optimizer in ("sgd", "adam8"):
-            if ev is not None:
-                ev[0].record(stream)
-            if args.optimizer == "sgd":
-                run.step_sgd(sgd_hp)  # fused kernel(s) and the commit
-            else:
-                run.step_adam8()      # one fused kernel per shard and the commit
-            if ev is not None:
-                ev[1].record(stream)
-            return
-        if not clip:
-            if ev is not None:
-                ev[0].record(stream)
-            run.reduce_adam_all()   # the fused kernels of every stepped shard (grouped launches)
-            if ev is not None:
-                ev[1].record(stream)
-        else:
-            with torch.cuda.stream(stream):
-                run.sqnorm.zero_()
-            if ev is not None:
-                ev[0].record(stream)
-            binding.zero_shard_grad_sqnorm_all_async(run.views, w.n_d, run.sqnorm, run.ctrl,
-                                                     g_dev=run.gbuf if run.gbuf else None, stream=stream)
-            if ev is not None:
-                ev[2].record(stream)
-            binding.zero_shard_clipped_adam_all_async(run.views, w.n_d, run.hp, args.clip, run.sqnorm, run.ctrl,
-                                                      g_dev=run.gbuf if run.gbuf else None, stream=stream)
-            if ev is not None:
-                ev[1].record(stream)
-        run.commit()
-
-    # untimed pre-warm: the first seconds of sustained HBM traffic after idle
-    # run a few percent slower; the timed region should see the steady state
-    t0 = time.perf_counter()
-    prewarm_steps = 0
-    while time.perf_counter() - t0 < args.prewarm_s:
-        for _ in range(10):
-            one_step()
-        prewarm_steps += 10
-        torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    lay = lay_scalars.cpu().tolist()
-    assert lay[4] == 0 and lay[2] == run.S, lay
-
-    pairs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    sampler.start()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches0 = binding.zero_kernel_launches()
-    t_start.record(stream)
-    for k in range(args.steps):
-        one_step(pairs[k])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    launches = binding.zero_kernel_launches() - launches0
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    ms_total = t_start.elapsed_time(t_end)
-    kern_ms = [ev[0].elapsed_time(ev[1]) for ev in pairs]
-    if clip:
-        norm_ms = [ev[0].elapsed_time(ev[2]) for ev in pairs]
-        upd_ms = [ev[2].elapsed_time(ev[1]) for ev in pairs]
-    ctrl = run.ctrl_host()
-    assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + args.warmup + args.steps, ctrl
-
-    ms_max = zdist.max_over_ranks(ms_total, device=dev)
+    res = time_steps(args, run, w, stream, world, args.steps, args.warmup, args.prewarm_s, local)
+    ms_max, kern_ms, ctrl = res["ms_max"], res["kern_ms"], res["ctrl"]
+    prewarm_steps = res["prewarm_steps"]
     elems = run.elements_per_step()
     total_elems = elems * world
     value = total_elems * args.steps / (ms_max / 1e3) / 1e9
@@ -543,6 +620,7 @@ def main():
         # contributions, writes g if kept; pass 2 reads g or re-reduces)
         b1 = (2 * w.n_d + (4 if run.gbuf else 0)) * elems
         b2 = ((4 if run.gbuf else 2 * w.n_d) + 26) * elems
+        norm_ms, upd_ms = res["norm_ms"], res["upd_ms"]
         clip_info = {"max_norm": args.clip, "keep_g": bool(run.gbuf),
                      "bytes_per_param": (2 * w.n_d + 34) if run.gbuf else (4 * w.n_d + 26),
                      "norm_pass": {"ms_mean": round(statistics.mean(norm_ms), 5),
@@ -569,10 +647,14 @@ def main():
         f"pct_of_{peak_kind}_peak": round(100 * hbm_gbs / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "group_step_kernel" if len(run.views) > 1 else "shard_step_kernel", "peak_kind": peak_kind,
+                     "kernel": ("group_step_kernel" if len(run.views) > 1 else "shard_step_kernel")
+                     + (" + restore_kernel" if not args.qwz else " + commit_kernel"),
+                     "peak_kind": peak_kind,
                      "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_min": round(min(kern_ms), 5)},
-        "clocks": clocks,
-        "gpu_launches": int(launches),
+        "clocks": res["clocks"],
+        "gpu_launches": int(res["launches"]),
+        "partition": {"kernel_us": round(part_us, 2), "fragments": part_frags,
+                      "when": "once per job, before the timed steps (zero_partition_layout_device)"},
         "e2e": e2e,
     }
     if args.optimizer == "sgd":
@@ -596,7 +678,7 @@ def main():
         line["qwz"] = {"block": 256, "extra_bytes_per_param": round(1 + 4 / 256, 4)}
     if clip_info is not None:
         line["clip"] = clip_info
-        line["roofline"]["kernel"] = "grad_norm_kernel + clipped_step_kernel"
+        line["roofline"]["kernel"] = "grad_norm_kernel + clipped_step_kernel + commit_kernel"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         opt = args.optimizer
         ns = oracle_sample(opt, elems)
@@ -615,6 +697,24 @@ def main():
         line["cpu_native"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th,
                               "kind": "zero_shard_step_cpu (ZeRO-Offload step on the host cores)",
                               "sample": f"{ns:,} params x N_d={w.n_d}, {steps} steps in {el:.1f} s"}
+
+    # the other target configurations of the same step, each on its own
+    # buffers after the previous ones are freed, timed the same way
+    extras = [x for x in args.extra_configs.split(",") if x and x != args.workload]
+    if extras and args.optimizer == "adam" and not clip and not args.qwz and not args.shard_params:
+        del run
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["configs"] = {}
+        for name in extras:
+            w2, run2 = make_runner(synth.WORKLOADS[name], stream)
+            res2 = time_steps(args, run2, w2, stream, world, args.steps, args.warmup,
+                              min(args.prewarm_s, 2.0), local)
+            res2["world"] = world
+            line["configs"][name] = workload_summary(args, w2, run2, res2, peak, peak_kind)
+            del run2
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
