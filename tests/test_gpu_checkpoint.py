@@ -11,8 +11,13 @@ from zero_partitioned_mixed_partition_gb300.runner import WorkloadRunner
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("qwz", [False, True])
 @pytest.mark.parametrize("n_d", [4, 16])
-def test_save_load_resume_is_exact(zs, cuda_device, n_d):
+def test_save_load_resume_is_exact(zs, cuda_device, n_d, qwz):
+    """qwz: every runner keeps the int8 qwZ copy of its fp16 slice; after
+    load() the copy must describe the loaded slice (the resumed runner's copy
+    was made from other weights), and after 2 more steps it must equal the
+    straight run's bit for bit."""
     n = 2048 * 9 + 5
     w = synth.Workload(name="ckpt", numels=(n * n_d,), n_d=n_d, rank=0, align=1, steps=5, lr=1e-3, beta1=0.9,
                        beta2=0.999, eps=1e-8, weight_decay=0.01, loss_scale=1024.0, grad_dist="normal",
@@ -27,13 +32,19 @@ def test_save_load_resume_is_exact(zs, cuda_device, n_d):
             run.step()
         torch.cuda.synchronize()
 
-    straight = WorkloadRunner(w, cuda_device)
+    def runner():
+        run = WorkloadRunner(w, cuda_device)
+        if qwz:
+            run.enable_qwz()
+        return run
+
+    straight = runner()
     run_steps(straight, [1, 2, 3, 4, 5])
-    first = WorkloadRunner(w, cuda_device)
+    first = runner()
     run_steps(first, [1, 2, 3])
     ckpt = first.save()
     del first
-    resumed = WorkloadRunner(w, cuda_device)
+    resumed = runner()
     for pair in resumed.state[0][:3]:           # scribble over the fresh state: load must replace it
         for t in pair:
             t.fill_(7.0)
@@ -41,18 +52,29 @@ def test_save_load_resume_is_exact(zs, cuda_device, n_d):
     resumed.step()                              # and advance its control block
     torch.cuda.synchronize()
     resumed.load(ckpt)
+    if qwz:                                     # the copy now describes the loaded slice
+        codes, scales = resumed.qwz[0]
+        ref_codes = torch.zeros_like(codes)
+        ref_scales = torch.zeros_like(scales)
+        zs.zero_qwz_quantize(resumed.state[0][3], resumed.n_valid[0], ref_codes, ref_scales)
+        torch.cuda.synchronize()
+        assert torch.equal(codes, ref_codes) and torch.equal(scales, ref_scales)
     run_steps(resumed, [4, 5])
     a, b = straight.ctrl_host(), resumed.ctrl_host()
     assert a == b and a["step"] == 4 and a["skipped"] == 1 and a["loss_scale"] == 512.0
     for x, y in zip(straight.current(0), resumed.current(0)):
         assert torch.equal(x, y)
+    if qwz:
+        for x, y in zip(straight.qwz[0], resumed.qwz[0]):
+            assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("n_d", [4, 16])
+@pytest.mark.parametrize("n_d", [4, 16, 32])
 def test_adam8_save_load_resume_is_exact(zs, cuda_device, n_d):
     """The same with 8-bit Adam state: the committed codes and block scales
     travel with the checkpoint, and 3 + 2 steps equal 5 straight steps bit for
-    bit (codes, scales, master, params, control block)."""
+    bit (codes, scales, master, params, control block).  n_d = 4 runs the
+    staged 8-element kernel, 16 the direct one, 32 the 16-element one."""
     n = 2048 * 9 + 5
     w = synth.Workload(name="ckpt8", numels=(n * n_d,), n_d=n_d, rank=0, align=1, steps=5, lr=1e-3, beta1=0.9,
                        beta2=0.999, eps=1e-8, weight_decay=0.01, loss_scale=1024.0, grad_dist="normal",

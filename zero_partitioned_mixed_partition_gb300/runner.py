@@ -221,7 +221,8 @@ class WorkloadRunner:
     def load(self, ckpt: dict):
         """Restore a save() of a runner of the same workload: the state goes
         into the set the saved control block names, the control block is
-        copied back as bytes."""
+        copied back as bytes; with a qwZ copy (enable_qwz), the copy is
+        re-quantized from the loaded fp16 slices."""
         ctrl = ckpt["ctrl"]
         self.ctrl.copy_(ctrl.to(self.device))
         cur = binding.read_ctrl(self.ctrl)["cur"]
@@ -237,6 +238,13 @@ class WorkloadRunner:
             for r, saved in ckpt["adam8"].items():
                 for pair, t in zip(self.adam8[r], saved):
                     pair[cur].copy_(t.to(self.device))
+        if getattr(self, "qwz", None):
+            # the int8 copy is a function of the fp16 slice: rebuild it from
+            # the loaded slice so no reader sees the old weights' codes
+            torch.cuda.synchronize(self.device)
+            for r in ckpt["shards"]:
+                codes, scales = self.qwz[r]
+                binding.zero_qwz_quantize(self.state[r][3], self.n_valid[r], codes, scales, stream=self.stream)
         torch.cuda.synchronize(self.device)
 
     # ------------------------------------------------------------ accounting --
