@@ -72,6 +72,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-offload", action="store_true",
+                    help="skip the ZeRO-Offload step (device -> host -> device) measurement")
+    ap.add_argument("--offload-params", type=int, default=96_000_000,
+                    help="parameters of the rank's shard the ZeRO-Offload measurement steps")
     ap.add_argument("--extra-configs", default="7b5,gpt2s",
                     help="other workloads timed in the same run after the main one (fp32 Adam step only), "
                          "reported under 'configs'; '' for none")
@@ -343,6 +347,74 @@ def native_cpu_throughput(w, n_sample: int, seconds: float, threads: int):
         if el >= seconds:
             break
     return n_sample * steps / el / 1e9, steps, el, threads
+
+
+def offload_throughput(run, w, n_sample: int, steps: int, threads: int):
+    """The ZeRO-Offload step with its transfers (zero_shard_step_offload) on
+    the first n_sample parameters of the rank's shard: the contributions come
+    from the runner's device buffers, the fp32 state lives in host memory, the
+    fp16 parameters go to a device buffer; two CUDA streams for the two link
+    directions.  Wall-clock per synchronous step after one untimed step.
+    Returns a dict for the JSON line."""
+    import torch
+    from zero_partitioned_mixed_partition_gb300 import binding, synth
+    r = run.shard_ids[0]
+    n = min(n_sample, run.n_valid[r])
+    dev = run.device
+    grads_dev = [g[:n] for g in run.grads[r]]
+    grads_host = [torch.empty(n, dtype=torch.float16).pin_memory() for _ in range(w.n_d)]
+    params_host = torch.empty(n, dtype=torch.float16).pin_memory()
+    params_dev = torch.empty(n, dtype=torch.float16, device=dev)
+    master = (synth.master_init(w, n, shard=r), torch.zeros(n))
+    m = (torch.zeros(n), torch.zeros(n))
+    v = (torch.zeros(n), torch.zeros(n))
+    view = binding.OffloadShardView(grads_dev, params_dev, grads_host, params_host, master, m, v, n)
+    hp = binding.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    d2h, h2d = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    cur = 0
+    for k in range(steps + 1):
+        if k == 1:
+            t0 = time.perf_counter()
+        ovf = binding.zero_shard_step_offload(view, w.n_d, hp, w.loss_scale, k + 1, cur, n_threads=threads,
+                                              d2h_stream=d2h, h2d_stream=h2d)
+        assert ovf == 0
+        cur ^= 1
+    el = time.perf_counter() - t0
+    ms = el / steps * 1e3
+    d2h_b, h2d_b = 2 * w.n_d * n, 2 * n
+    return {"value": round(n / (ms / 1e3) / 1e9, 4), "unit": "Gparams/s", "ms_per_step": round(ms, 3),
+            "shard_params": n, "cores": threads, "steps": steps,
+            "link_bytes_per_step": {"d2h": d2h_b, "h2d": h2d_b},
+            "link_gbs": {"d2h": round(d2h_b / (ms / 1e3) / 1e9, 1), "h2d": round(h2d_b / (ms / 1e3) / 1e9, 1)},
+            "pages_link_bytes_per_step": 4 * n,
+            "path": "zero_shard_step_offload: N_d fp16 contributions device -> pinned host, the step on the host "
+                    "cores (fp32 state in host memory), fp16 params pinned host -> device; chunked, both link "
+                    "directions and the host arithmetic overlapped",
+            "note": "the pages' 4 Psi per step is fp16 grads down + fp16 params up for one rank's model "
+                    "(N_d = 1); with N_d simulated ranks the N_d contributions cross instead of the reduced "
+                    "gradient: 2 N_d + 2 bytes per parameter"}
+
+
+def host_copy_gbs(threads: int, nbytes: int = 1 << 30) -> float:
+    """Host memory bandwidth ceiling: PyTorch's parallel CPU copy of a 1 GiB
+    fp32 tensor on `threads` threads, read + write bytes, best of 5."""
+    import torch
+    prev = torch.get_num_threads()
+    torch.set_num_threads(threads)
+    try:
+        a = torch.ones(nbytes // 4, dtype=torch.float32)
+        b = torch.empty_like(a)
+        b.copy_(a)
+        best = None
+        for _ in range(5):
+            t0 = time.perf_counter()
+            b.copy_(a)
+            el = time.perf_counter() - t0
+            best = el if best is None else min(best, el)
+        return 2 * nbytes / best / 1e9
+    finally:
+        torch.set_num_threads(prev)
 
 
 def reference_arm(args, rank: int):
@@ -694,9 +766,15 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.optimizer == "adam" and not clip:
         ns = min(32_000_000, elems)
         g, steps, el, th = native_cpu_throughput(w, ns, 3.0, os.cpu_count() or 1)
+        ceiling = host_copy_gbs(th)
         line["cpu_native"] = {"value": round(g, 4), "unit": "Gparams/s", "cores": th,
                               "kind": "zero_shard_step_cpu (ZeRO-Offload step on the host cores)",
-                              "sample": f"{ns:,} params x N_d={w.n_d}, {steps} steps in {el:.1f} s"}
+                              "sample": f"{ns:,} params x N_d={w.n_d}, {steps} steps in {el:.1f} s",
+                              "host_gbs": round(g * step_bytes_per_param("adam", w.n_d), 1),
+                              "host_copy_gbs": round(ceiling, 1),
+                              "frac_of_host_copy": round(g * step_bytes_per_param("adam", w.n_d) / ceiling, 3)}
+        if not args.no_offload:
+            line["offload"] = offload_throughput(run, w, args.offload_params, 3, th)
 
     # the other target configurations of the same step, each on its own
     # buffers after the previous ones are freed, timed the same way

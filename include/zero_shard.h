@@ -536,6 +536,57 @@ ZS_API int32_t zero_shard_step_cpu(const zs_shard* shards, int32_t n_shards, int
                                    const zs_adam* hp, double loss_scale, int64_t step, int32_t cur,
                                    int32_t n_threads, int32_t* overflow_out);
 
+/* One rank's shard for the ZeRO-Offload step with its transfers.
+ *   grads_dev    HOST array of n_d DEVICE pointers: the rank's n-element
+ *                slices of the n_d fp16 gradient contributions (rank order)
+ *   params_dev   DEVICE fp16 slice of the full parameter buffer (n elements)
+ *                that receives the updated parameters
+ *   grads_host   HOST array of n_d page-locked HOST staging buffers of n fp16
+ *                elements each (cudaHostAlloc / cudaHostRegister)
+ *   params_host  page-locked HOST staging buffer of n fp16 elements
+ *   master, m, v two sets of HOST fp32 state (n elements each), set cur read,
+ *                set cur ^ 1 written, as for zero_shard_step_cpu
+ *   n            elements of the shard (>= 0)
+ * The caller owns every buffer; the library allocates no memory (it creates
+ * and destroys one CUDA event per chunk within the call). */
+typedef struct zs_offload_shard {
+    const uint16_t* const* grads_dev;
+    uint16_t* params_dev;
+    uint16_t* const* grads_host;
+    uint16_t* params_host;
+    float* master[2];
+    float* m[2];
+    float* v[2];
+    int64_t n;
+} zs_offload_shard;
+
+/* ZeRO-Offload's step of one rank: the gradients cross the link to the host,
+ * the host cores run the Adam step on the host-resident fp32 state, and the
+ * new fp16 parameters cross back.  The shard is cut into chunks of `chunk`
+ * elements (0: 4,194,304; else a multiple of 16): every contribution of every
+ * chunk is copied device -> host on d2h_stream (one cudaMemcpyAsync per
+ * contribution and chunk), n_threads host threads (0 = all cores) step each
+ * chunk as soon as its copies have landed, and each finished chunk's fp16
+ * parameters are copied host -> device on h2d_stream while later chunks are
+ * still crossing or being stepped.  Pass two different streams so both link
+ * directions run at once.  Arithmetic, ping-pong, overflow test and restore as
+ * zero_shard_step_cpu, bit for bit; after an overflow the fp16 slice is sent
+ * again from the kept master weights.  Synchronous: on return the device slice
+ * holds the step's (or, after an overflow, the kept) parameters, and
+ * *overflow_out (HOST) gets 0 or 1; the caller commits as for zero_shard_step.
+ * Link bytes per step: 2 n_d n device -> host and 2 n host -> device (2 n more
+ * after an overflow).  ZS_ERR_ARG for a bad argument or staging memory that is
+ * not page-locked (text in zero_last_error()); ZS_ERR_CUDA for a failed copy
+ * or event.
+ * Source: "DeepSpeed ZeRO Stages", sec. 5.1 (ZeRO-Offload: optimizer state and
+ * step on the CPU, transfers overlapped); "DeepSpeed ZeRO: Extreme Memory
+ * Efficiency", "Offloading the optimizer entirely: ZeRO-Offload" (fp16
+ * gradients down and fp16 parameters up each step, 4 Psi bytes at N_d = 1). */
+ZS_API int32_t zero_shard_step_offload(const zs_offload_shard* shard, int32_t n_d, const zs_adam* hp,
+                                       double loss_scale, int64_t step, int32_t cur, int32_t n_threads,
+                                       int64_t chunk, void* d2h_stream, void* h2d_stream,
+                                       int32_t* overflow_out);
+
 /* ------------------------------------------------------------------------ */
 /* Quantized weights (qwZ) on their own.                                     */
 /* ------------------------------------------------------------------------ */

@@ -61,6 +61,11 @@ class Adam8Shard(ctypes.Structure):
                 ("m_scale", _P * 2), ("v_scale", _P * 2), ("params", _P), ("n", _I64)]
 
 
+class OffloadShard(ctypes.Structure):
+    _fields_ = [("grads_dev", ctypes.POINTER(_P)), ("params_dev", _P), ("grads_host", ctypes.POINTER(_P)),
+                ("params_host", _P), ("master", _P * 2), ("m", _P * 2), ("v", _P * 2), ("n", _I64)]
+
+
 class Sgd(ctypes.Structure):
     _fields_ = [("lr", _F64), ("momentum", _F64), ("weight_decay", _F64)]
 
@@ -98,6 +103,7 @@ _SIGNATURES = {
     "zero_step_commit_async": (_I32, [_P, _I32, _P, _P, _P]),
     "zero_params_from_master": (_I32, [_P, _P, _I64, _P]),
     "zero_shard_step_cpu": (_I32, [_P, _I32, _I32, _P, _F64, _I64, _I32, _I32, _P]),
+    "zero_shard_step_offload": (_I32, [_P, _I32, _P, _F64, _I64, _I32, _I32, _I64, _P, _P, _P]),
     "zero_shard_step_sgd_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "zero_shard_step_adam8_async": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "zero_adam8_maps": (_I32, [_P, _P]),
@@ -469,6 +475,51 @@ def zero_shard_step_cpu(shards: Sequence[ShardView], n_d: int, hp: Adam, loss_sc
     rc = lib().zero_shard_step_cpu(arr, len(shards), int(n_d), ctypes.byref(hp), float(loss_scale), int(step),
                                    int(cur), int(n_threads), ctypes.byref(ovf))
     _check(rc, "zero_shard_step_cpu")
+    return int(ovf.value)
+
+
+class OffloadShardView:
+    """One rank's shard for the ZeRO-Offload step: the device contributions
+    and fp16 slice, page-locked host staging buffers for both, and the host
+    fp32 state (two sets each of master, m, v)."""
+
+    def __init__(self, grads_dev, params_dev, grads_host, params_host, master, m, v, n):
+        def host(t, dtype, what, pinned=False):
+            if t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+                raise TypeError(f"{what}: expected a contiguous host {dtype} tensor")
+            if pinned and not t.is_pinned():
+                raise TypeError(f"{what}: expected page-locked host memory (pin_memory())")
+            return t.data_ptr()
+        self.n = int(n)
+        self.grads_dev, self.grads_host = list(grads_dev), list(grads_host)
+        self.params_dev, self.params_host = params_dev, params_host
+        self.master, self.m, self.v = tuple(master), tuple(m), tuple(v)
+        self._dev = (_P * max(len(self.grads_dev), 1))(*[_dev_ptr(g, torch.float16, "grads_dev")
+                                                          for g in self.grads_dev])
+        self._host = (_P * max(len(self.grads_host), 1))(*[host(g, torch.float16, "grads_host", True)
+                                                           for g in self.grads_host])
+        self.struct = OffloadShard()
+        self.struct.grads_dev = ctypes.cast(self._dev, ctypes.POINTER(_P))
+        self.struct.grads_host = ctypes.cast(self._host, ctypes.POINTER(_P))
+        self.struct.params_dev = _dev_ptr(params_dev, torch.float16, "params_dev")
+        self.struct.params_host = host(params_host, torch.float16, "params_host", True)
+        for i in range(2):
+            self.struct.master[i] = host(self.master[i], torch.float32, "master")
+            self.struct.m[i] = host(self.m[i], torch.float32, "m")
+            self.struct.v[i] = host(self.v[i], torch.float32, "v")
+        self.struct.n = self.n
+
+
+def zero_shard_step_offload(shard: OffloadShardView, n_d: int, hp: Adam, loss_scale: float, step: int, cur: int,
+                            n_threads: int = 0, chunk: int = 0, d2h_stream=None, h2d_stream=None) -> int:
+    """ZeRO-Offload step: contributions to the host, the step on the host
+    cores, fp16 parameters back to the device, overlapped by chunks; returns
+    the overflow flag (synchronous)."""
+    ovf = _I32(-1)
+    rc = lib().zero_shard_step_offload(ctypes.byref(shard.struct), int(n_d), ctypes.byref(hp), float(loss_scale),
+                                       int(step), int(cur), int(n_threads), int(chunk), _stream(d2h_stream),
+                                       _stream(h2d_stream), ctypes.byref(ovf))
+    _check(rc, "zero_shard_step_offload")
     return int(ovf.value)
 
 

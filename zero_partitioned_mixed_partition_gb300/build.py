@@ -91,5 +91,20 @@ def build_all(force: bool = False) -> tuple:
         return a.result(), b.result()
 
 
+def host_vectorization_report() -> str:
+    """The host compiler's report on the loops of the host-core step
+    (csrc/cpu_step.cpp) it vectorized, compiled with the library's own flags
+    plus -fopt-info-vec-optimized; one line per vectorized loop."""
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-Xcompiler", "-fopt-info-vec-optimized", "-c",
+               os.path.join(CSRC, "cpu_step.cpp"), "-o", os.path.join(d, "cpu_step.o")]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"compile failed:\n{r.stdout}\n{r.stderr}")
+    lines = [ln for ln in (r.stdout + r.stderr).splitlines() if "cpu_step.cpp" in ln and "vectorized" in ln]
+    return "\n".join(sorted(set(lines), key=lambda ln: int(ln.split(":")[1]) if ln.split(":")[1].isdigit() else 0))
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))
