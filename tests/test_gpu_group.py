@@ -63,7 +63,12 @@ CASES = {
 
 @pytest.mark.parametrize("case", sorted(CASES))
 @pytest.mark.parametrize("math", ["ieee", "fast"])
-def test_grouped_equals_per_shard_and_oracle(zs, oracle, cuda_device, case, math):
+@pytest.mark.parametrize("path", ["split", "async"])
+def test_grouped_equals_per_shard_and_oracle(zs, oracle, cuda_device, case, math, path):
+    """path = split: the grouped fused launches, then the commit kernel; async:
+    zero_shard_step_async, whose last launch commits the step itself (the
+    cases with several launches check that an overflow seen by an earlier
+    launch reaches the last one's commit)."""
     n_d, sizes, misaligned, qwz = CASES[case]
     w = _workload(n_d, seed=len(sizes) + n_d)
     mode = zs.ZS_MATH_FAST if math == "fast" else zs.ZS_MATH_IEEE
@@ -86,8 +91,11 @@ def test_grouped_equals_per_shard_and_oracle(zs, oracle, cuda_device, case, math
             host_step = [[synth.fp16_bits(t) for t in v.grads] for v in va]
         else:
             host_step = host
-        zs.zero_shard_reduce_adam_all_async(va, n_d, hp, ca)       # grouped
-        zs.zero_step_commit_async(va, hp, ca)
+        if path == "split":
+            zs.zero_shard_reduce_adam_all_async(va, n_d, hp, ca)   # grouped
+            zs.zero_step_commit_async(va, hp, ca)
+        else:
+            zs.zero_shard_step_async(va, n_d, hp, ca)              # grouped, commit in the last launch
         for v in vb:                                                 # one launch per shard
             zs.zero_shard_reduce_adam_async(v, n_d, hp, cb)
         zs.zero_step_commit_async(vb, hp, cb)

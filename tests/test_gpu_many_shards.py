@@ -45,11 +45,15 @@ def _build(zs, oracle, dev, w, sizes):
     return views, host, refs, state
 
 
+@pytest.mark.parametrize("victim", ["first", "last"])
 @pytest.mark.parametrize("path", ["async", "sync"])
-def test_max_shards_one_step(zs, oracle, cuda_device, path):
+def test_max_shards_one_step(zs, oracle, cuda_device, path, victim):
+    """victim: the overflow is planted in the first launch of the step (shard 1)
+    or in its last (the last shard); either way every shard skips."""
     rng = np.random.Generator(np.random.PCG64(21))
     sizes = [int(x) for x in rng.integers(0, 700, zs.ZS_MAX_SHARDS)]
     sizes[0], sizes[17], sizes[-1] = 0, 1, 513        # empty, single, ragged last shard
+    sizes[1] = max(sizes[1], 400)
     w = _workload(3)
     views, host, refs, state = _build(zs, oracle, cuda_device, w, sizes)
     hp = zs.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
@@ -57,7 +61,7 @@ def test_max_shards_one_step(zs, oracle, cuda_device, path):
     zs.zero_ctrl_init(ctrl, w.loss_scale)
     flag = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     ls, applied, cur = w.loss_scale, 0, 0
-    last = len(sizes) - 1
+    last = len(sizes) - 1 if victim == "last" else 1
     for step in range(1, 4):
         inject = step == 2
         if inject:

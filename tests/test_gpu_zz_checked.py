@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["test_gpu_step.py", "test_gpu_layout.py", "test_gpu_clip.py", "test_gpu_sgd.py", "test_gpu_qwz.py",
           "test_gpu_fast_math.py", "test_gpu_many_shards.py", "test_gpu_group.py", "test_gpu_guard.py",
-          "test_gpu_checkpoint.py", "test_gpu_adam8.py"]
+          "test_gpu_checkpoint.py", "test_gpu_adam8.py", "test_zz_no_alloc.py"]
 
 
 def test_parity_suites_under_index_checks(zs, cuda_device):
