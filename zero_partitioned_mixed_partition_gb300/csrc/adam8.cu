@@ -255,7 +255,8 @@ adam8_step_kernel(const __grid_constant__ A8Args<CAP, G> p) {
     __shared__ Maps sm;
     __shared__ Coef s_coef;
     __shared__ int s_cur;
-    __shared__ float s_red[2][2][kWarps];  // [iteration parity][m, v][warp]
+    static_assert(kWarps % 4 == 0, "the warps' maxima are read four at a time");
+    __shared__ __align__(16) uint32_t s_red[2][2][kWarps];  // [iteration parity][m, v][warp]: bit patterns
     {
         // the tables: word copy of the parameter block into shared memory
         constexpr int kWords = (int)(sizeof(Maps) / 4);
@@ -379,30 +380,33 @@ adam8_step_kernel(const __grid_constant__ A8Args<CAP, G> p) {
                     Mem<1>::store_h(p.params[sh] + e + j, &th[j]);
                 }
         }
-        // the block's largest |m'| and v'
+        // the block's largest |m'| and v': the thread's maxima (fmaxf, which
+        // passes over a NaN), then one warp reduction each on their bit
+        // patterns (for floats >= 0 the largest pattern is the largest value),
+        // then the warps' maxima from shared memory, read as 16-byte vectors
         float am = 0.0f, av = 0.0f;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             am = fmaxf(am, fabsf(m[j]));
             av = fmaxf(av, v[j]);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-            av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, o));
-        }
+        const uint32_t am_w = __reduce_max_sync(0xffffffffu, __float_as_uint(am));
+        const uint32_t av_w = __reduce_max_sync(0xffffffffu, __float_as_uint(av));
         if (lane == 0) {
-            s_red[par][0][warp] = am;
-            s_red[par][1][warp] = av;
+            s_red[par][0][warp] = am_w;
+            s_red[par][1][warp] = av_w;
         }
         __syncthreads();  // one barrier per block: a parity slot is not rewritten before every warp read it
-        am = s_red[par][0][0];
-        av = s_red[par][1][0];
+        uint32_t am_b = 0u, av_b = 0u;
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) {
-            am = fmaxf(am, s_red[par][0][w]);
-            av = fmaxf(av, s_red[par][1][w]);
+        for (int w = 0; w < kWarps; w += 4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(&s_red[par][0][w]);
+            const uint4 b = *reinterpret_cast<const uint4*>(&s_red[par][1][w]);
+            am_b = max(am_b, max(max(a.x, a.y), max(a.z, a.w)));
+            av_b = max(av_b, max(max(b.x, b.y), max(b.z, b.w)));
         }
+        am = __uint_as_float(am_b);
+        av = __uint_as_float(av_b);
         // codes of x = m' / am and v' / av, each quotient rounded once: by the
         // constant-divisor division when both scales allow it (the block's
         // scales are the same in every thread, so the branch is uniform), else
