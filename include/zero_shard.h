@@ -174,7 +174,8 @@ typedef struct zs_ctrl {
     int32_t cur;           /* state set (0/1) that holds the committed state */
     int32_t overflow;      /* OR of the non-finite tests of the step in flight */
     int32_t last_overflow; /* overflow flag of the last finished step */
-    uint32_t arrivals;     /* internal block counter of the commit kernel; 0 between steps */
+    uint32_t arrivals;     /* internal block counter of the step's end (the commit kernel, or the
+                              last fused launch of zero_shard_step_async); 0 between steps */
 } zs_ctrl;
 
 /* ------------------------------------------------------------------------ */
