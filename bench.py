@@ -589,7 +589,9 @@ def workload_summary(args, w, run, res, peak, peak_kind):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": ("group_step_kernel" if len(run.views) > 1 else "shard_step_kernel")
                          + " + restore_kernel", "peak_kind": peak_kind,
-                         "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_min": round(min(res["kern_ms"]), 5)},
+                         "kernel_ms_mean": round(mean_kern_ms, 5),
+                         "kernel_ms_median": round(statistics.median(res["kern_ms"]), 5),
+                         "kernel_ms_min": round(min(res["kern_ms"]), 5)},
             "clocks": res["clocks"], "gpu_launches": int(res["launches"]),
             "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
             if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number"}
@@ -722,7 +724,8 @@ def main():
                      "kernel": ("group_step_kernel" if len(run.views) > 1 else "shard_step_kernel")
                      + (" + restore_kernel" if not args.qwz else " + commit_kernel"),
                      "peak_kind": peak_kind,
-                     "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_min": round(min(kern_ms), 5)},
+                     "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_median": round(statistics.median(kern_ms), 5),
+                     "kernel_ms_min": round(min(kern_ms), 5)},
         "clocks": res["clocks"],
         "gpu_launches": int(res["launches"]),
         "partition": {"kernel_us": round(part_us, 2), "fragments": part_frags,
