@@ -15,9 +15,16 @@
 //     float x with |x| <= d (both signs), the codes of div_by_constant(x, d,
 //     RN(1/d)) under both maps equal the codes of __fdiv_rn(x, d), and the two
 //     quotients are equal bit for bit wherever |x / d| >= 2^-27.
+//  4. the mixed-precision accumulation of a contribution (add_f16x2 in
+//     csrc/step_common.cuh: PTX add.rn.f32.f16 on each half of a word) against
+//     widening with __half2float and adding with __fadd_rn, bit for bit (NaN
+//     against NaN), for every fp16 value in both halves and 4096 fp32
+//     accumulators (zeros of both signs, fp16 extremes, subnormals, values
+//     near the fp16 range and spread over the fp32 range).
 //
 // Every loop is a grid-stride loop over a fixed range; nothing waits.  Prints
 // one line per check and exits 1 if any value differs.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -25,9 +32,12 @@
 #include <cmath>
 #include <cstring>
 
+#include "zero_shard.h"
+
 namespace {
 
 #include "adam8_math.cuh"
+#include "step_common.cuh"
 
 struct Result {
     unsigned long long bad;
@@ -117,6 +127,26 @@ __global__ void scale_check(float d, const float* thr7, const uint8_t* b7, const
             atomicAdd(&out->bad, 1ull);
             atomicMin(&out->first, (unsigned long long)b);
         }
+    }
+}
+
+__global__ void mixed_add_check(const float* accs, int na, Result* out) {
+    const uint32_t hb = blockIdx.x * blockDim.x + threadIdx.x;  // every fp16 bit pattern
+    if (hb > 0xffffu) return;
+    unsigned long long bad = 0;
+    for (int i = 0; i < na; ++i) {
+        float a0 = accs[i], a1 = accs[(i + 7) % na];
+        const uint32_t h1 = hb ^ 0x8000u;  // the other sign in the high half
+        const float r0 = __fadd_rn(a0, __half2float(__ushort_as_half((unsigned short)hb)));
+        const float r1 = __fadd_rn(a1, __half2float(__ushort_as_half((unsigned short)h1)));
+        add_f16x2(hb | (h1 << 16), a0, a1);
+        const bool nan0 = r0 != r0 && a0 != a0, nan1 = r1 != r1 && a1 != a1;
+        if ((__float_as_uint(a0) != __float_as_uint(r0) && !nan0) || (__float_as_uint(a1) != __float_as_uint(r1) && !nan1))
+            ++bad;
+    }
+    if (bad) {
+        atomicAdd(&out->bad, bad);
+        atomicMin(&out->first, (unsigned long long)hb);
     }
 }
 
@@ -214,6 +244,31 @@ int main() {
         char name[96];
         snprintf(name, sizeof(name), "block quotient, scale 0x%08x = %.9g, every |x| <= scale", bits, d);
         run(name, [&] { scale_check<<<blocks, threads>>>(d, d_thr7, d_b7, d_thr8, d_b8, d_res); });
+    }
+    // accumulators for the mixed add: special values, then a fixed linear
+    // congruential sequence (every fourth near the fp16 range)
+    {
+        constexpr int na = 4096;
+        static float accs[na];
+        const float special[] = {0.0f, -0.0f, 1.0f, -1.0f, 65504.0f, -65504.0f, 1e-8f, -1e-8f, 3.0e38f, 1e-40f,
+                                 -1e-40f, 5.96e-8f, 0.5f};
+        int k = 0;
+        for (float v : special) accs[k++] = v;
+        uint32_t r = 12345u;
+        for (; k < na; ++k) {
+            r = r * 1664525u + 1013904223u;
+            uint32_t bits = r;
+            if ((k & 3) == 0) bits = (bits & 0x80FFFFFFu) | (((112u + (r >> 27)) & 0xFFu) << 23);
+            float f;
+            std::memcpy(&f, &bits, 4);
+            if (!std::isfinite(f)) f = 1.0f;
+            accs[k] = f;
+        }
+        float* d_accs;
+        if (cudaMalloc(&d_accs, sizeof(accs))) return fail("cudaMalloc");
+        cudaMemcpy(d_accs, accs, sizeof(accs), cudaMemcpyHostToDevice);
+        run("mixed-precision add, every fp16 value x 4096 accumulators",
+            [&] { mixed_add_check<<<256, 256>>>(d_accs, na, d_res); });
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return fail("kernels");
     printf("%s\n", status == 0 ? "all equal" : "MISMATCH");

@@ -10,7 +10,9 @@ program tests/gpu_adam8_math_check.cu (compiled here for sm_103a):
 - the normalization of a block by its scale (the same division by the
   block's largest magnitude) against the IEEE quotient: equal codes under
   both maps for every |x| <= scale, equal quotients wherever they reach a
-  code threshold, for 40 scales over [2^-64, 2^64]."""
+  code threshold, for 40 scales over [2^-64, 2^64];
+- the mixed-precision accumulation of an fp16 contribution (PTX
+  add.rn.f32.f16) against widening and __fadd_rn, for every fp16 value."""
 import os
 import shutil
 import subprocess
@@ -33,4 +35,4 @@ def test_adam8_math_exhaustive(cuda_device, tmp_path):
     print(r.stdout)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("all equal")
-    assert r.stdout.count("0 mismatches") == 4 + 40 + 40
+    assert r.stdout.count("0 mismatches") == 4 + 40 + 40 + 1

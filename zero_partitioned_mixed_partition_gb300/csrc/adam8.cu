@@ -144,7 +144,7 @@ __device__ __forceinline__ void a8_load_global(const A8Args<CAP, G>& p, int sh, 
     Codes<VEC>::load(p.vq[sh][cur] + e, cv);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
-    sum_contributions<CAP, VEC, ND>(p.grads[sh], p.n_d, e, acc);
+    sum_contributions<CAP, VEC, ND, true>(p.grads[sh], p.n_d, e, acc);
 }
 
 // the first `valid` (0..VEC) elements, one at a time; zeros past them (which
@@ -161,7 +161,7 @@ __device__ __forceinline__ void a8_load_partial(const A8Args<CAP, G>& p, int sh,
             th[j] = __ldcs(p.master[sh][cur] + e + j);
             cm[j] = p.mq[sh][cur][e + j];
             cv[j] = p.vq[sh][cur][e + j];
-            sum_contributions<CAP, 1, ND>(p.grads[sh], p.n_d, e + j, &acc[j]);
+            sum_contributions<CAP, 1, ND, true>(p.grads[sh], p.n_d, e + j, &acc[j]);
         }
     }
 }
@@ -214,10 +214,11 @@ __device__ __forceinline__ void a8_load_staged(const A8Args<CAP, G>& p, const un
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
 #pragma unroll 4
     for (int k = 0; k < nd; ++k) {   // rank order, as sum_contributions
-        float h[8];
-        Mem<16>::load_h8(reinterpret_cast<const uint16_t*>(st + ((int64_t)k * kStageThreads + t) * 16), h);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], h[j]);
+        const uint4 r = *reinterpret_cast<const uint4*>(st + ((int64_t)k * kStageThreads + t) * 16);
+        add_f16x2(r.x, acc[0], acc[1]);
+        add_f16x2(r.y, acc[2], acc[3]);
+        add_f16x2(r.z, acc[4], acc[5]);
+        add_f16x2(r.w, acc[6], acc[7]);
     }
     const unsigned char* s = st + (int64_t)nd * kStageThreads * 16;
     const float4 a = *reinterpret_cast<const float4*>(s + t * 16);

@@ -137,6 +137,11 @@ __device__ __forceinline__ void adam_update(const Coef& c, float gs, float& th, 
 template <int VEC> struct Mem;
 
 template <> struct Mem<8> {
+    // the 8 fp16 values as raw words (two per word, the lower address in the low half)
+    static __device__ __forceinline__ void load_h_words(const uint16_t* p, uint32_t* w) {
+        const uint4 r = __ldcs(reinterpret_cast<const uint4*>(p));
+        w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+    }
     static __device__ __forceinline__ void load_h(const uint16_t* p, float* out) {
         const uint4 r = __ldcs(reinterpret_cast<const uint4*>(p));
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
@@ -169,6 +174,12 @@ template <> struct Mem<8> {
 };
 
 template <> struct Mem<16> {
+    static __device__ __forceinline__ void load_h_words(const uint16_t* p, uint32_t* w) {
+        const uint4 a = *reinterpret_cast<const uint4*>(p);
+        const uint4 b = *reinterpret_cast<const uint4*>(p + 8);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
     static __device__ __forceinline__ void load_h8(const uint16_t* p, float* out) {
         const uint4 r = *reinterpret_cast<const uint4*>(p);
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
@@ -226,21 +237,49 @@ template <> struct Mem<1> {
     }
 };
 
+// acc0 += fp16 value in the low half of w, acc1 += the one in the high half,
+// each as one mixed-precision add (PTX add.rn.f32.f16, sm_100 and later): the
+// fp16 operand is widened exactly and the sum rounded once to fp32, the
+// result of widening first and adding with __fadd_rn, without the separate
+// conversion instruction.
+__device__ __forceinline__ void add_f16x2(uint32_t w, float& acc0, float& acc1) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(w));
+}
+__device__ __forceinline__ void add_f16(uint16_t h, float& acc) {
+    asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(h));
+}
+
 // Unroll of the contribution loop when N_d is a compile-time constant above 16.
 constexpr int kUnrollLargeNd = 8;
 
 // Sum of the N_d contributions of VEC consecutive elements, in rank order.
+// MIXED: each contribution added by the mixed-precision add (add_f16x2), the
+// same sums; the issue-bound 8-bit Adam kernel takes it (+1.5 % on the 1.5B
+// shard), the HBM-bound kernels do not (the fp32 step measured 9-11 % slower
+// with it at N_d = 4 and 64).
 // ND > 0: exactly ND contributions, known at compile time (fully unrolled for
 // ND <= 16, unrolled by kUnrollLargeNd above); ND == 0: p.n_d of them (<= CAP),
 // unrolled by 4.
-template <int CAP, int VEC, int ND>
+template <int CAP, int VEC, int ND, bool MIXED = false>
 __device__ __forceinline__ void sum_contributions(const uint16_t* const (&grads)[CAP], int n_d, int64_t e,
                                                   float* acc) {
     auto add = [&](int k) {
-        float h[VEC];
-        Mem<VEC>::load_h(grads[k] + e, h);
+        if constexpr (MIXED && VEC == 1) {
+            add_f16(__ldcs(reinterpret_cast<const unsigned short*>(grads[k] + e)), acc[0]);
+        } else if constexpr (MIXED) {
+            uint32_t w[VEC / 2];
+            Mem<VEC>::load_h_words(grads[k] + e, w);
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[j] = __fadd_rn(acc[j], h[j]);
+            for (int j = 0; j < VEC / 2; ++j) add_f16x2(w[j], acc[2 * j], acc[2 * j + 1]);
+        } else {
+            float h[VEC];
+            Mem<VEC>::load_h(grads[k] + e, h);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc[j] = __fadd_rn(acc[j], h[j]);
+        }
     };
     if constexpr (ND > 0 && ND <= 16) {
 #pragma unroll
