@@ -53,7 +53,7 @@ extern "C" {
 #define ZS_ERR_ARG (-1)     /* invalid argument; nothing was enqueued */
 #define ZS_ERR_ALIGN (-2)   /* a pointer is not aligned to its element type */
 #define ZS_ERR_CUDA (-3)    /* a CUDA call failed; see zero_last_error() */
-#define ZS_ERR_TIMEOUT (-4) /* reserved: no kernel of this library waits */
+#define ZS_ERR_TIMEOUT (-4) /* reserved: no kernel of this library polls a flag */
 
 /* Largest data-parallel degree (number of gradient contributions). */
 #define ZS_MAX_ND 1024

@@ -264,3 +264,33 @@ def test_adam8_struct_layout(zs):
     assert zs.Adam8Shard.params.offset == 88 and zs.Adam8Shard.n.offset == 96
     text = open(os.path.join(ROOT, "include", "zero_shard.h")).read()
     assert re.search(r"#define ZS_ADAM8_BLOCK 2048\b", text) and zs.ZS_ADAM8_BLOCK == 2048
+
+
+def test_offload_argument_checks_refuse_before_cuda(zs):
+    """zero_shard_step_offload validates on the host before any CUDA call: a
+    NULL shard, a chunk that is not a multiple of 16, a negative n, bad
+    hyper-parameters; an empty shard returns at once with no overflow."""
+    import ctypes
+    L = zs.lib()
+    ovf = ctypes.c_int32(-1)
+    hp = zs.adam(1e-3)
+    s = zs.OffloadShard()
+    s.n = 0
+    call = lambda shard, n_d=2, h=hp, ls=1.0, step=1, cur=0, threads=0, chunk=0: L.zero_shard_step_offload(
+        shard, n_d, ctypes.byref(h), ls, step, cur, threads, chunk, None, None, ctypes.byref(ovf))
+    assert call(None) == zs.ZS_ERR_ARG
+    assert call(ctypes.byref(s), chunk=10) == zs.ZS_ERR_ARG
+    assert call(ctypes.byref(s), n_d=0) == zs.ZS_ERR_ARG
+    assert call(ctypes.byref(s), ls=0.0) == zs.ZS_ERR_ARG
+    assert call(ctypes.byref(s), step=0) == zs.ZS_ERR_ARG
+    assert call(ctypes.byref(s), cur=2) == zs.ZS_ERR_ARG
+    assert call(ctypes.byref(s), threads=-1) == zs.ZS_ERR_ARG
+    bad = zs.adam(1e-3, beta1=1.5)
+    assert call(ctypes.byref(s), h=bad) == zs.ZS_ERR_ARG
+    s.n = -1
+    assert call(ctypes.byref(s)) == zs.ZS_ERR_ARG
+    s.n = 8                                          # buffers missing
+    assert call(ctypes.byref(s)) == zs.ZS_ERR_ARG
+    s.n = 0
+    ovf.value = -1
+    assert call(ctypes.byref(s)) == zs.ZS_OK and ovf.value == 0
