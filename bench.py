@@ -37,6 +37,8 @@ METRIC = "Gparams/s and achieved HBM GB/s (% of GB300 peak) of the ZeRO shard Ad
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
+ROOFLINE_DURATION = ("the timed region's time per step (the step's launches back to back, gaps included); "
+                     "kernel_ms_*: an event pair around each step in a second pass of as many steps")
 
 
 def parse_args():
@@ -513,14 +515,22 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = binding.zero_kernel_launches()
+    # the timed region: the steps back to back, nothing else on the stream
     t_start.record(stream)
-    for k in range(steps):
-        one_step(pairs[k])
+    for _ in range(steps):
+        one_step()
     t_end.record(stream)
     torch.cuda.synchronize()
     launches = binding.zero_kernel_launches() - launches0
     if world > 1:
         dist.barrier()
+    # then as many steps again with an event pair around each (and around each
+    # pass of the clipped step): the per-launch durations.  Events between the
+    # launches keep the next step from being scheduled while the current one
+    # drains, so this pass is not the timed region.
+    for k in range(steps):
+        one_step(pairs[k])
+    torch.cuda.synchronize()
     clocks = sampler.stop()
     ms_total = t_start.elapsed_time(t_end)
     out = {"ms_total": ms_total, "kern_ms": [ev[0].elapsed_time(ev[1]) for ev in pairs],
@@ -529,7 +539,7 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
         out["norm_ms"] = [ev[0].elapsed_time(ev[2]) for ev in pairs]
         out["upd_ms"] = [ev[2].elapsed_time(ev[1]) for ev in pairs]
     ctrl = run.ctrl_host()
-    assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + warmup + steps, ctrl
+    assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + warmup + 2 * steps, ctrl
     out["ctrl"] = ctrl
     out["ms_max"] = zdist.max_over_ranks(ms_total, device=torch.device("cuda", local))
     return out
@@ -574,8 +584,11 @@ def workload_summary(args, w, run, res, peak, peak_kind):
     bytes_step = run.bytes_per_step()
     value = elems * world * steps / (res["ms_max"] / 1e3) / 1e9
     hbm_gbs = bytes_step * world * steps / (res["ms_max"] / 1e3) / 1e9
+    # roofline over the timed region: its time per step, every microsecond of
+    # it charged to the step's launches
+    step_ms = res["ms_max"] / steps
+    achieved = bytes_step / (step_ms / 1e3) / 1e9
     mean_kern_ms = statistics.mean(res["kern_ms"])
-    achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
     traffic = None
     per = recorded_traffic("adam")
     if per and w.n_d in per:
@@ -589,9 +602,11 @@ def workload_summary(args, w, run, res, peak, peak_kind):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": ("group_step_kernel" if len(run.views) > 1 else "shard_step_kernel")
                          + " + restore_kernel", "peak_kind": peak_kind,
+                         "duration": ROOFLINE_DURATION, "step_ms": round(step_ms, 5),
                          "kernel_ms_mean": round(mean_kern_ms, 5),
                          "kernel_ms_median": round(statistics.median(res["kern_ms"]), 5),
-                         "kernel_ms_min": round(min(res["kern_ms"]), 5)},
+                         "kernel_ms_min": round(min(res["kern_ms"]), 5),
+                         "frac_per_launch_events": round(bytes_step / (mean_kern_ms / 1e3) / 1e9 / peak, 4)},
             "clocks": res["clocks"], "gpu_launches": int(res["launches"]),
             "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB); no flush"
             if bytes_step > L2_BYTES else "inputs fit in L2: not an HBM number"}
@@ -665,10 +680,11 @@ def main():
         bytes_step += sum(run.n_valid[r] + 4 * ((run.n_valid[r] + 255) // 256) for r in run.shard_ids)
     hbm_gbs = bytes_step * world * args.steps / (ms_max / 1e3) / 1e9
     if args.log_steps:
-        # one record per timed step; no step of the timed region overflowed
-        # (checked above), so t advances by one per step and L is constant
+        # one record per step of the per-launch pass that follows the timed
+        # region; no step overflowed (checked above), so t advances by one per
+        # step and L is constant
         peak_gbs, _ = measured_peaks()
-        t_first = prewarm_steps + args.warmup + 1
+        t_first = prewarm_steps + args.warmup + args.steps + 1
         path = args.log_steps if world == 1 else f"{args.log_steps}.rank{rank}"
         with open(path, "w") as f:
             for k, ms in enumerate(kern_ms):
@@ -680,9 +696,11 @@ def main():
                                     "pct_of_peak": round(100 * gbs / peak_gbs, 2)}) + "\n")
     peak, peak_kind = measured_peaks()
 
-    # roofline of the dominant kernel: algorithmic bytes per launch / mean launch time
+    # roofline of the step: algorithmic bytes per step / the timed region's
+    # time per step (back-to-back launches; the gaps between them count too)
+    step_ms = ms_max / args.steps
+    achieved = bytes_step / (step_ms / 1e3) / 1e9
     mean_kern_ms = statistics.mean(kern_ms)
-    achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
     traffic = None
     if args.optimizer in TRAFFIC_RECORDS and not clip and not args.qwz:
         traffic_per_param = recorded_traffic(args.optimizer)
@@ -724,8 +742,10 @@ def main():
                      "kernel": ("group_step_kernel" if len(run.views) > 1 else "shard_step_kernel")
                      + (" + restore_kernel" if not args.qwz else " + commit_kernel"),
                      "peak_kind": peak_kind,
+                     "duration": ROOFLINE_DURATION, "step_ms": round(step_ms, 5),
                      "kernel_ms_mean": round(mean_kern_ms, 5), "kernel_ms_median": round(statistics.median(kern_ms), 5),
-                     "kernel_ms_min": round(min(kern_ms), 5)},
+                     "kernel_ms_min": round(min(kern_ms), 5),
+                     "frac_per_launch_events": round(bytes_step / (mean_kern_ms / 1e3) / 1e9 / peak, 4)},
         "clocks": res["clocks"],
         "gpu_launches": int(res["launches"]),
         "partition": {"kernel_us": round(part_us, 2), "fragments": part_frags,
@@ -740,7 +760,7 @@ def main():
         if instr and w.n_d in instr:
             # the N_d <= 4 kernel is bound by instruction issue, not HBM: its
             # issue roofline, from the ncu-counted instructions per parameter
-            rate = instr[w.n_d] * elems / (mean_kern_ms / 1e3)
+            rate = instr[w.n_d] * elems / (step_ms / 1e3)
             line["roofline_issue"] = {"bound": "alu", "achieved": round(rate / 1e12, 3),
                                       "peak": round(ISSUE_PEAK_TINSTR_S / 1e12, 3), "unit": "T thread-instr/s",
                                       "frac": round(rate / ISSUE_PEAK_TINSTR_S, 4),

@@ -787,14 +787,24 @@ int32_t launch_step_vec(const StepArgs<CAP>& a, bool pdl, cudaStream_t stream) {
                          "shard_step_kernel");
 }
 
-// ZS_MATH_FAST runs the FAST instantiation where it measured faster: the
-// 8-element layout (N_d = 4: +5.6 %, 6.76 TB/s) and the 16-element layout
-// compiled for N_d = 16, 32, 64 (+1.3 % at 16), without a qwZ copy (with one,
-// the 8-element kernel measured no gain: 172.4 vs 173.4 Gparams/s at N_d = 4).
+// ZS_MATH_FAST runs the FAST instantiation of the vector layouts without a
+// qwZ copy where it measured faster: the 8-element layout (N_d = 4: +5.6 %,
+// 6.76 TB/s), the 16-element layout compiled for N_d = 16, 32, 64 (+1.3 % at
+// 16), and the 16-element layout with a run-time N_d on launches of at most
+// kFastRuntimeWideMax elements.  That last kernel measured faster with FAST on
+// short launches and slower on long ones (N_d = 8, steps back to back: +5 % at
+// 8M and +2.5 % at 15.6M elements; -3 % at 24M and 32M, -2.3 % at 64M and
+// 100M, -1.5 % at 200M).  With a qwZ copy the 8-element kernel measured no
+// gain (172.4 vs 173.4 Gparams/s at N_d = 4).
+constexpr int64_t kFastRuntimeWideMax = (int64_t)1 << 24;
+
+template <int VEC, int ND>
+bool fast_pays(int64_t elements) { return VEC == 8 || ND > 0 || elements <= kFastRuntimeWideMax; }
+
 template <int CAP, int VEC, int ND, bool QZ>
 int32_t launch_math(const StepArgs<CAP>& a, bool fast, bool pdl, cudaStream_t stream) {
-    if constexpr (!QZ && (VEC == 8 || (VEC == 16 && ND > 0))) {
-        if (fast) return launch_step_vec<CAP, VEC, ND, QZ, true>(a, pdl, stream);
+    if constexpr (!QZ && (VEC == 8 || VEC == 16)) {
+        if (fast && fast_pays<VEC, ND>(a.n)) return launch_step_vec<CAP, VEC, ND, QZ, true>(a, pdl, stream);
     }
     return launch_step_vec<CAP, VEC, ND, QZ>(a, pdl, stream);
 }
@@ -907,9 +917,7 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
     if constexpr (ND == 0 || ND > 4) {
         if (vec == 16) {
             if (qz) return go(group_step_kernel<CAP, 16, ND, true, false>);
-            if constexpr (ND > 0) {
-                if (fast) return go(group_step_kernel<CAP, 16, ND, false, true>);
-            }
+            if (fast && fast_pays<16, ND>(a.vstart[count] * 16)) return go(group_step_kernel<CAP, 16, ND, false, true>);
             return go(group_step_kernel<CAP, 16, ND, false, false>);
         }
     }
