@@ -1,10 +1,10 @@
-"""ZeRO-Offload on the GPU box ("DeepSpeed ZeRO Stages" sec. 5.1; "DeepSpeed
+"""ZeRO-Offload on a GB300 machine ("DeepSpeed ZeRO Stages" sec. 5.1; "DeepSpeed
 ZeRO: Extreme Memory Efficiency", the ZeRO-Offload section): the host-core
 step and the full offload step with its transfers, against the oracle, bit
 for bit.
 
-  - the host-core step (zero_shard_step_cpu) on this machine's own CPU (the GPU
-    box's host is aarch64, this build machine x86_64): ragged sizes,
+  - the host-core step (zero_shard_step_cpu) on the GPU machine's own host
+    CPU (aarch64 on Grace; the CPU tests run it on x86_64 too): ragged sizes,
     N_d = 1, 4, 64, one thread and every core, an overflow step;
   - zero_shard_step_offload: contributions copied from the device to
     page-locked staging, the step on the host cores, fp16 parameters copied
