@@ -146,8 +146,8 @@ def measured_peaks():
 # Per step kind: the committed DRAM-traffic record of its dominant kernel and
 # the sources that kernel is compiled from (the record holds their digest).
 TRAFFIC_RECORDS = {
-    "adam": ("shard_step_kernel_traffic.txt", ("shard_step.cu", "step_common.cuh")),
-    "adam8": ("adam8_step_kernel_traffic.txt", ("adam8.cu", "adam8_math.cuh", "step_common.cuh")),
+    "adam": ("shard_step_kernel_traffic.txt", ("shard_step.cu", "step_common.cuh", "step_end.cuh")),
+    "adam8": ("adam8_step_kernel_traffic.txt", ("adam8.cu", "adam8_math.cuh", "step_common.cuh", "step_end.cuh")),
 }
 
 
@@ -459,9 +459,10 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
 
     One step is the whole hot path over the stepped shards: the fused
     reduce + overflow test + Adam + fp16 cast launches and the end of the step
-    (for the fp32 Adam step, the last fused launch commits and a restore
-    kernel follows that leaves at once unless the step overflowed; the other
-    kinds end with the commit kernel).  Returns a dict of the measurements."""
+    (for the fp32 Adam, SGD and 8-bit Adam steps, the last fused launch
+    commits and a restore kernel follows that leaves at once unless the step
+    overflowed; the clipped step and a step with a qwZ copy end with the
+    commit kernel).  Returns a dict of the measurements."""
     import torch
     import torch.distributed as dist
     from zero_partitioned_mixed_partition_gb300 import binding
@@ -477,9 +478,9 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
         if ev is not None:
             ev[0].record(stream)
         if args.optimizer == "sgd":
-            run.step_sgd(sgd_hp)      # fused kernel(s) and the commit
+            run.step_sgd(sgd_hp)      # fused kernel(s) ending the step, then the restore check
         elif args.optimizer == "adam8":
-            run.step_adam8()          # fused kernel(s) and the commit
+            run.step_adam8()          # fused kernel(s) ending the step, then the restore check
         elif not clip:
             run.step()                # fused kernel(s) ending the step, then the restore check
         else:
@@ -753,8 +754,9 @@ def main():
         "e2e": e2e,
     }
     if args.optimizer == "sgd":
-        line["optimizer"] = {"kind": "sgd", "momentum": 0.9, "timed": "fused kernel + commit"}
-        line["roofline"]["kernel"] = ("sgd_group_kernel" if len(run.views) > 1 else "sgd_step_kernel") + " + commit_kernel"
+        line["optimizer"] = {"kind": "sgd", "momentum": 0.9,
+                             "timed": "fused kernel(s), the last ending the step, + restore check"}
+        line["roofline"]["kernel"] = ("sgd_group_kernel" if len(run.views) > 1 else "sgd_step_kernel") + " + restore_kernel"
     if args.optimizer == "adam8":
         instr = recorded_instructions("adam8")
         if instr and w.n_d in instr:
@@ -767,8 +769,8 @@ def main():
                                       "instructions_per_param": instr[w.n_d], "source": "ncu, recorded"}
         line["optimizer"] = {"kind": "adam8", "block": binding.ZS_ADAM8_BLOCK,
                              "state": "fp32 master, uint8 codes of m and v, fp32 scale per block (ping-pong)",
-                             "timed": "fused kernel per shard + commit"}
-        line["roofline"]["kernel"] = "adam8_step_kernel + commit_kernel"
+                             "timed": "fused kernel(s), the last ending the step, + restore check"}
+        line["roofline"]["kernel"] = "adam8_step_kernel + restore_kernel"
     if args.qwz:
         line["qwz"] = {"block": 256, "extra_bytes_per_param": round(1 + 4 / 256, 4)}
     if clip_info is not None:

@@ -175,7 +175,8 @@ typedef struct zs_ctrl {
     int32_t overflow;      /* OR of the non-finite tests of the step in flight */
     int32_t last_overflow; /* overflow flag of the last finished step */
     uint32_t arrivals;     /* internal block counter of the step's end (the commit kernel, or the
-                              last fused launch of zero_shard_step_async); 0 between steps */
+                              last fused launch of zero_shard_step_async, _sgd_async or
+                              _adam8_async); 0 between steps */
 } zs_ctrl;
 
 /* ------------------------------------------------------------------------ */
@@ -450,8 +451,14 @@ ZS_API int32_t zero_params_from_master(const float* master_dev, uint16_t* params
  *   theta' = theta - lr b',  params = fp16_rn(theta')
  * The momentum b lives in zs_shard.m (both sets; b starts at 0), zs_shard.v
  * is unused (may be NULL) and qcodes must be NULL.  Loss scale and the
- * ping-pong set come from *ctrl_dev; one fused kernel per shard, then the
- * device commit.  Per element 2 n_d + 18 bytes.
+ * ping-pong set come from *ctrl_dev; consecutive shards of one access width
+ * are stepped up to 16 per launch; the step's last launch ends it in the
+ * control block (its last block to finish commits or skips, as
+ * zero_step_commit_async decides, with beta1 = beta2 = 0 for the unused
+ * beta^t products) and one restore kernel follows that re-casts the fp16
+ * slices only after an overflow, both with programmatic serialization (a call
+ * with only empty shards ends in the commit kernel instead).  Per element
+ * 2 n_d + 18 bytes.
  * Source: "DeepSpeed ZeRO Stages", sec. 1.2 (mixed-precision SGD with momentum, K = 4). */
 ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                          const zs_sgd* hp, zs_ctrl* ctrl_dev, void* stream);
@@ -504,9 +511,11 @@ typedef struct zs_adam8_shard {
  *   with a non-zero magnitude code; v alike.
  * hp->math applies to u as in zero_shard_step; the codes do not depend on it.
  * Consecutive shards of one access width (empty shards join any group) are
- * stepped up to 16 per launch with n_d <= 64, one per launch above; then the
- * device commit (a skipped step leaves set cur, so codes and scales too,
- * untouched).  Per element 2 n_d + 14 bytes (+ 16 per block).
+ * stepped up to 16 per launch with n_d <= 64, one per launch above.  The
+ * step's last launch ends it in the control block and one restore kernel
+ * follows, as in zero_shard_step_sgd_async (a skipped step leaves set cur, so
+ * codes and scales too, untouched).  Per element 2 n_d + 14 bytes (+ 16 per
+ * block).
  * Source: "DeepSpeed ZeRO Stages", sec. 1.2 (8-bit Adam, K = 6), with the update of "ZeRO Stage 1
  * Math", "The per-step mechanics", beats 2-3. */
 ZS_API int32_t zero_shard_step_adam8_async(const zs_adam8_shard* shards, int32_t n_shards, int32_t n_d,

@@ -318,7 +318,7 @@ def test_adam8_grouped_launches(zs, oracle, cuda_device, n_d, sizes, misaligned)
             ref.compare(to_np(v.master[cur]), to_np(v.m_codes[cur]), to_np(v.v_codes[cur]), to_np(v.m_scale[cur][:nb]),
                         to_np(v.v_scale[cur][:nb]), f16_bits(v.params), exact=True,
                         what=f"n_d={n_d} shard {i} step {step}")
-    # one launch per group: runs of one width, at most 16 shards each, plus the commit
+    # one launch per group: runs of one width, at most 16 shards each, plus the restore pass
     live = [i for i, n in enumerate(sizes) if n]
     groups, i = 0, 0
     widths = [0 if k in misaligned else 1 for k in range(len(sizes))]

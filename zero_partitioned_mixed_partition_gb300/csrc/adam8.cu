@@ -17,6 +17,10 @@
 // 2 N_d + 6 bytes are read and 8 written (+ 16 bytes per block for the scales).
 // One launch steps up to 16 shards of a step, their blocks back to back; up to
 // N_d = 4 each thread prefetches its share of the next block with cp.async.
+// The step ends as the fp32 step does: the last block of the step's last
+// launch commits or skips in the control block and the restore pass follows;
+// the launches carry programmatic serialization, and each CTA copies the code
+// tables to shared memory before it waits for the kernel ahead of it.
 //
 // The nearest-code search: the map values, and for each pair of neighbours the
 // largest float not above their midpoint (so `x > t` decides "nearer to the
@@ -39,6 +43,7 @@
 namespace {
 
 #include "step_common.cuh"
+#include "step_end.cuh"
 
 // index-check sites of this file (the shared ones are 1-9)
 [[maybe_unused]] constexpr uint32_t kSiteAdam8 = 10, kSiteAdam8Scale = 11;
@@ -126,6 +131,7 @@ struct A8Args {
     zs_adam hp;
     const zs_ctrl* ctrl;  // loss scale, t and the ping-pong set
     int32_t* flag;        // &ctrl->overflow
+    zs_ctrl* commit;      // non-null: this launch ends the step (arrive_and_finish)
     Maps maps;
 };
 
@@ -266,6 +272,9 @@ adam8_step_kernel(const __grid_constant__ A8Args<CAP, G> p) {
         uint32_t* dst = reinterpret_cast<uint32_t*>(&sm);
         for (int i = threadIdx.x; i < kWords; i += kThr) dst[i] = src[i];
     }
+    // the tables come from the kernel parameters; global memory only from here
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         const zs_ctrl* ctrl = p.ctrl;
         const double p1 = __dmul_rn(ctrl->beta1_pow, p.hp.beta1);  // beta^(t+1)
@@ -450,7 +459,11 @@ adam8_step_kernel(const __grid_constant__ A8Args<CAP, G> p) {
         }
     }
     if constexpr (STAGED) copies_wait<0>();  // (the last group is empty) nothing in flight at exit
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        if (any_bad) atomicOr(p.flag, 1);
+        if (p.commit != nullptr) arrive_and_finish(p.commit, gridDim.x, p.hp.beta1, p.hp.beta2);
+    }
 }
 
 // ------------------------------------------------------------------ launch ---
@@ -524,14 +537,14 @@ int32_t launch_a8(const A8Args<CAP, G>& a, cudaStream_t stream) {
         smem = (size_t)(2 * stage_bytes(ND > 0 ? ND : a.n_d));
     }
     const int blocks = a8_blocks(k, threads, smem, a.bstart[a.n_shards]);
-    adam8_step_kernel<CAP, G, VEC, ND, FAST, VECLOAD, STAGED><<<blocks, threads, smem, stream>>>(a);
-    return zs::check_launch("adam8_step_kernel");
+    return launch_ex(adam8_step_kernel<CAP, G, VEC, ND, FAST, VECLOAD, STAGED>, blocks, threads, smem, true, stream, a,
+                     "adam8_step_kernel");
 }
 
 // One launch for `count` (<= G) consecutive shards of one access width.
 template <int CAP, int G, int ND>
 int32_t launch_a8_cap(const zs_adam8_shard* shards, int count, int32_t n_d, int width, const zs_adam& hp,
-                      zs_ctrl* ctrl, cudaStream_t stream) {
+                      zs_ctrl* ctrl, zs_ctrl* commit, cudaStream_t stream) {
     A8Args<CAP, G> a;
     a.bstart[0] = 0;
     for (int g = 0; g < G; ++g) {
@@ -555,6 +568,7 @@ int32_t launch_a8_cap(const zs_adam8_shard* shards, int count, int32_t n_d, int 
     a.hp = hp;
     a.ctrl = ctrl;
     a.flag = &ctrl->overflow;
+    a.commit = commit;
     a.maps = host_maps().maps;
     const bool fast = hp.math == ZS_MATH_FAST;
     // Up to 4 contributions: the staged 8-element kernel.  5-16: the direct
@@ -580,24 +594,24 @@ int32_t launch_a8_cap(const zs_adam8_shard* shards, int count, int32_t n_d, int 
 // Shards per launch: up to kA8GroupMax with at most 64 contributions (the
 // pointer tables stay within the kernel parameter space), one above.
 int32_t launch_a8_group(const zs_adam8_shard* shards, int count, int32_t n_d, int width, const zs_adam& hp,
-                        zs_ctrl* ctrl, cudaStream_t stream) {
+                        zs_ctrl* ctrl, zs_ctrl* commit, cudaStream_t stream) {
     switch (n_d) {
-    case 16: return launch_a8_cap<16, kA8GroupMax, 16>(shards, count, n_d, width, hp, ctrl, stream);
-    case 32: return launch_a8_cap<32, kA8GroupMax, 32>(shards, count, n_d, width, hp, ctrl, stream);
-    case 64: return launch_a8_cap<64, kA8GroupMax, 64>(shards, count, n_d, width, hp, ctrl, stream);
+    case 16: return launch_a8_cap<16, kA8GroupMax, 16>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    case 32: return launch_a8_cap<32, kA8GroupMax, 32>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    case 64: return launch_a8_cap<64, kA8GroupMax, 64>(shards, count, n_d, width, hp, ctrl, commit, stream);
     default: break;
     }
     // a lone shard with up to 16 contributions: the one-slot kernel, whose
     // block walk needs no shard lookup (xl, N_d = 4: 203.5 Gparams/s against
     // 193.6 for the 16-slot kernel stepping one shard)
     if (n_d <= 4)
-        return count == 1 ? launch_a8_cap<4, 1, 0>(shards, count, n_d, width, hp, ctrl, stream)
-                          : launch_a8_cap<4, kA8GroupMax, 0>(shards, count, n_d, width, hp, ctrl, stream);
+        return count == 1 ? launch_a8_cap<4, 1, 0>(shards, count, n_d, width, hp, ctrl, commit, stream)
+                          : launch_a8_cap<4, kA8GroupMax, 0>(shards, count, n_d, width, hp, ctrl, commit, stream);
     if (n_d <= 16)
-        return count == 1 ? launch_a8_cap<16, 1, 0>(shards, count, n_d, width, hp, ctrl, stream)
-                          : launch_a8_cap<16, kA8GroupMax, 0>(shards, count, n_d, width, hp, ctrl, stream);
-    if (n_d <= 64) return launch_a8_cap<64, kA8GroupMax, 0>(shards, count, n_d, width, hp, ctrl, stream);
-    return launch_a8_cap<ZS_MAX_ND, 1, 0>(shards, count, n_d, width, hp, ctrl, stream);
+        return count == 1 ? launch_a8_cap<16, 1, 0>(shards, count, n_d, width, hp, ctrl, commit, stream)
+                          : launch_a8_cap<16, kA8GroupMax, 0>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    if (n_d <= 64) return launch_a8_cap<64, kA8GroupMax, 0>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    return launch_a8_cap<ZS_MAX_ND, 1, 0>(shards, count, n_d, width, hp, ctrl, commit, stream);
 }
 
 }  // namespace
@@ -635,25 +649,34 @@ ZS_API int32_t zero_shard_step_adam8_async(const zs_adam8_shard* shards, int32_t
     // consecutive shards of one access width (empty ones join any group): up
     // to kA8GroupMax per launch with n_d <= 64, one per launch above
     const int group_max = n_d <= 64 ? kA8GroupMax : 1;
-    int32_t i = 0;
+    struct Range { int32_t first, count; };
+    Range plan[ZS_MAX_SHARDS];
+    int32_t np = 0, i = 0;
     while (i < n_shards) {
         if (shards[i].n == 0) { ++i; continue; }
         int32_t j = i + 1;
         while (j < n_shards && j - i < group_max && (shards[j].n == 0 || width[j] == width[i])) ++j;
-        const int32_t rc = launch_a8_group(shards + i, j - i, n_d, width[i], *hp, ctrl_dev, st);
-        if (rc != ZS_OK) return rc;
+        plan[np++] = Range{i, j - i};
         i = j;
     }
-    zs_shard commit[ZS_MAX_SHARDS];
-    for (int32_t i = 0; i < n_shards; ++i) {
-        // the commit restores params from master[cur] on an overflow; it reads nothing else
-        std::memset(&commit[i], 0, sizeof(zs_shard));
-        commit[i].master[0] = shards[i].master[0];
-        commit[i].master[1] = shards[i].master[1];
-        commit[i].params = shards[i].params;
-        commit[i].n = shards[i].n;
+    // the last launch finishes the step in the control block
+    for (int32_t k = 0; k < np; ++k) {
+        const int32_t rc = launch_a8_group(shards + plan[k].first, plan[k].count, n_d, width[plan[k].first], *hp,
+                                           ctrl_dev, k + 1 == np ? ctrl_dev : nullptr, st);
+        if (rc != ZS_OK) return rc;
     }
-    return zs::launch_commit(commit, n_shards, *hp, ctrl_dev, st);
+    zs_shard ends[ZS_MAX_SHARDS];
+    for (int32_t s = 0; s < n_shards; ++s) {
+        // the restore pass (and the commit kernel) re-cast params from
+        // master[cur] after an overflow; they read nothing else
+        std::memset(&ends[s], 0, sizeof(zs_shard));
+        ends[s].master[0] = shards[s].master[0];
+        ends[s].master[1] = shards[s].master[1];
+        ends[s].params = shards[s].params;
+        ends[s].n = shards[s].n;
+    }
+    if (np > 0) return zs::launch_restore_pass(ends, n_shards, ctrl_dev, st);
+    return zs::launch_commit(ends, n_shards, *hp, ctrl_dev, st);  // nothing launched: the commit kernel ends it
 }
 
 }  // extern "C"

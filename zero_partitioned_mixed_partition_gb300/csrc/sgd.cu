@@ -6,8 +6,10 @@
 // unscaled, tested for non-finite values, and the update
 //   d = g + wd theta,  b' = mu b + d,  theta' = theta - lr b'
 // runs on the fp32 master and momentum (ping-pong, read set cur, write cur ^ 1)
-// with the fp16 cast, every fp32 operation rounded once.  The device commit
-// of the Adam step is reused (its beta^t bookkeeping is unused here).
+// with the fp16 cast, every fp32 operation rounded once.  The step ends as the
+// Adam step does: the last block of the step's last launch commits or skips
+// in the control block (its beta^t bookkeeping is unused here), and the
+// restore pass follows; the launches carry programmatic serialization.
 // Per element: 2 N_d + 8 bytes read, 8 + 2 written.
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -17,6 +19,7 @@
 namespace {
 
 #include "step_common.cuh"
+#include "step_end.cuh"
 
 // Threads per block: 512 for the 16-element layout with 32 or more
 // contributions (CAP >= 32), which at its ~80 registers puts exactly one block
@@ -39,6 +42,7 @@ struct SgdArgs {
     double lr, momentum, weight_decay;
     const zs_ctrl* ctrl;  // loss scale and the ping-pong set
     int32_t* flag;        // &ctrl->overflow
+    zs_ctrl* commit;      // non-null: this launch ends the step (arrive_and_finish)
 };
 
 // VEC elements of one shard starting at element e (grads / n_d: its
@@ -73,6 +77,8 @@ template <int CAP, int VEC, int ND>
 __global__ void __launch_bounds__(sgd_threads<VEC, CAP>()) sgd_step_kernel(const __grid_constant__ SgdArgs<CAP> p) {
     __shared__ float s_inv;
     __shared__ int s_cur;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         s_inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)p.n_d, p.ctrl->loss_scale)));
         s_cur = p.ctrl->cur;
@@ -96,7 +102,11 @@ __global__ void __launch_bounds__(sgd_threads<VEC, CAP>()) sgd_step_kernel(const
         if (blockIdx.x == 0 && e < p.n)
             bad |= sgd_elements<CAP, 1, ND>(p.grads, p.n_d, p.params, p.n, inv, lr, mu, wd, e, th_in, b_in, th_out, b_out);
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.flag, 1);
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        if (any_bad) atomicOr(p.flag, 1);
+        if (p.commit != nullptr) arrive_and_finish(p.commit, gridDim.x, 0.0, 0.0);
+    }
 }
 
 // Several shards of one step in one launch, as the Adam step's grouped kernel:
@@ -117,6 +127,7 @@ struct SgdGroupArgs {
     double lr, momentum, weight_decay;
     const zs_ctrl* ctrl;
     int32_t* flag;
+    zs_ctrl* commit;      // non-null: this launch ends the step (arrive_and_finish)
 };
 
 template <int CAP, int VEC, int ND>
@@ -124,6 +135,8 @@ __global__ void __launch_bounds__(sgd_threads<VEC, CAP>())
 sgd_group_kernel(const __grid_constant__ SgdGroupArgs<CAP> a) {
     __shared__ float s_inv;
     __shared__ int s_cur;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         s_inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)a.n_d, a.ctrl->loss_scale)));
         s_cur = a.ctrl->cur;
@@ -151,12 +164,16 @@ sgd_group_kernel(const __grid_constant__ SgdGroupArgs<CAP> a) {
                                                 a.mom[t][cur ^ 1]);
         }
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.flag, 1);
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        if (any_bad) atomicOr(a.flag, 1);
+        if (a.commit != nullptr) arrive_and_finish(a.commit, gridDim.x, 0.0, 0.0);
+    }
 }
 
 template <int CAP, int ND>
 int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl,
-                         cudaStream_t stream) {
+                         zs_ctrl* commit, cudaStream_t stream) {
     SgdGroupArgs<CAP> a;
     const bool wide = width == 2 && n_d > 4;
     const int vec = wide ? 16 : 8;
@@ -181,10 +198,10 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
     a.weight_decay = hp.weight_decay;
     a.ctrl = ctrl;
     a.flag = &ctrl->overflow;
+    a.commit = commit;
     auto go = [&](auto kernel, int threads) {
         const int blocks = zs::persistent_blocks((const void*)kernel, threads, a.vstart[count] > 0 ? a.vstart[count] : 1);
-        kernel<<<blocks, threads, 0, stream>>>(a);
-        return zs::check_launch("sgd_group_kernel");
+        return launch_ex(kernel, blocks, threads, 0, true, stream, a, "sgd_group_kernel");
     };
     if constexpr (ND == 0 || ND > 4) {
         if (wide) return go(sgd_group_kernel<CAP, 16, ND>, sgd_threads<16, CAP>());
@@ -193,16 +210,16 @@ int32_t launch_group_cap(const zs_shard* shards, int count, int32_t n_d, int wid
 }
 
 int32_t launch_group(const zs_shard* shards, int count, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl,
-                     cudaStream_t stream) {
+                     zs_ctrl* commit, cudaStream_t stream) {
     switch (n_d) {
-    case 16: return launch_group_cap<16, 16>(shards, count, n_d, width, hp, ctrl, stream);
-    case 32: return launch_group_cap<32, 32>(shards, count, n_d, width, hp, ctrl, stream);
-    case 64: return launch_group_cap<64, 64>(shards, count, n_d, width, hp, ctrl, stream);
+    case 16: return launch_group_cap<16, 16>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    case 32: return launch_group_cap<32, 32>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    case 64: return launch_group_cap<64, 64>(shards, count, n_d, width, hp, ctrl, commit, stream);
     default: break;
     }
-    if (n_d <= 4) return launch_group_cap<4, 0>(shards, count, n_d, width, hp, ctrl, stream);
-    if (n_d <= 16) return launch_group_cap<16, 0>(shards, count, n_d, width, hp, ctrl, stream);
-    return launch_group_cap<64, 0>(shards, count, n_d, width, hp, ctrl, stream);
+    if (n_d <= 4) return launch_group_cap<4, 0>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    if (n_d <= 16) return launch_group_cap<16, 0>(shards, count, n_d, width, hp, ctrl, commit, stream);
+    return launch_group_cap<64, 0>(shards, count, n_d, width, hp, ctrl, commit, stream);
 }
 
 template <int CAP, int VEC, int ND>
@@ -210,12 +227,11 @@ int32_t launch_vec(const SgdArgs<CAP>& a, cudaStream_t stream) {
     const void* k = (const void*)sgd_step_kernel<CAP, VEC, ND>;
     constexpr int threads = sgd_threads<VEC, CAP>();
     const int blocks = zs::persistent_blocks(k, threads, a.n / VEC > 0 ? a.n / VEC : 1);
-    sgd_step_kernel<CAP, VEC, ND><<<blocks, threads, 0, stream>>>(a);
-    return zs::check_launch("sgd_step_kernel");
+    return launch_ex(sgd_step_kernel<CAP, VEC, ND>, blocks, threads, 0, true, stream, a, "sgd_step_kernel");
 }
 
 template <int CAP, int ND>
-int32_t launch_cap(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl,
+int32_t launch_cap(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl, zs_ctrl* commit,
                    cudaStream_t stream) {
     SgdArgs<CAP> a;
     for (int k = 0; k < CAP; ++k) a.grads[k] = k < n_d ? s.grads[k] : nullptr;
@@ -231,6 +247,7 @@ int32_t launch_cap(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, 
     a.weight_decay = hp.weight_decay;
     a.ctrl = ctrl;
     a.flag = &ctrl->overflow;
+    a.commit = commit;
     if constexpr (ND == 0 || ND > 4) {
         if (width == 2 && n_d > 4) return launch_vec<CAP, 16, ND>(a, stream);
     }
@@ -238,17 +255,18 @@ int32_t launch_cap(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, 
     return launch_vec<CAP, 1, ND>(a, stream);
 }
 
-int32_t launch(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+int32_t launch(const zs_shard& s, int32_t n_d, int width, const zs_sgd& hp, zs_ctrl* ctrl, zs_ctrl* commit,
+               cudaStream_t stream) {
     switch (n_d) {
-    case 16: return launch_cap<16, 16>(s, n_d, width, hp, ctrl, stream);
-    case 32: return launch_cap<32, 32>(s, n_d, width, hp, ctrl, stream);
-    case 64: return launch_cap<64, 64>(s, n_d, width, hp, ctrl, stream);
+    case 16: return launch_cap<16, 16>(s, n_d, width, hp, ctrl, commit, stream);
+    case 32: return launch_cap<32, 32>(s, n_d, width, hp, ctrl, commit, stream);
+    case 64: return launch_cap<64, 64>(s, n_d, width, hp, ctrl, commit, stream);
     default: break;
     }
-    if (n_d <= 4) return launch_cap<4, 0>(s, n_d, width, hp, ctrl, stream);
-    if (n_d <= 16) return launch_cap<16, 0>(s, n_d, width, hp, ctrl, stream);
-    if (n_d <= 64) return launch_cap<64, 0>(s, n_d, width, hp, ctrl, stream);
-    return launch_cap<ZS_MAX_ND, 0>(s, n_d, width, hp, ctrl, stream);
+    if (n_d <= 4) return launch_cap<4, 0>(s, n_d, width, hp, ctrl, commit, stream);
+    if (n_d <= 16) return launch_cap<16, 0>(s, n_d, width, hp, ctrl, commit, stream);
+    if (n_d <= 64) return launch_cap<64, 0>(s, n_d, width, hp, ctrl, commit, stream);
+    return launch_cap<ZS_MAX_ND, 0>(s, n_d, width, hp, ctrl, commit, stream);
 }
 
 // Checks one SGD shard (v unused, no qwZ copy); *width as for the Adam step.
@@ -308,19 +326,31 @@ ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shard
     }
     cudaStream_t st = (cudaStream_t)stream;
     // consecutive shards with one vector width: up to 16 per grouped launch
-    int32_t i = 0;
+    struct Range { int32_t first, count; bool group; };
+    Range plan[ZS_MAX_SHARDS];
+    int32_t np = 0, i = 0;
     while (i < n_shards) {
         if (shards[i].n == 0) { ++i; continue; }
         const bool groupable = n_d <= 64 && width[i] >= 1;
         int32_t j = i + 1;
         if (groupable)
             while (j < n_shards && j - i < kSgdGroupMax && width[j] == width[i]) ++j;
-        int32_t rc = (groupable && j - i > 1) ? launch_group(shards + i, j - i, n_d, width[i], *hp, ctrl_dev, st)
-                                              : launch(shards[i], n_d, width[i], *hp, ctrl_dev, st);
-        if (rc != ZS_OK) return rc;
-        i = groupable ? j : i + 1;
+        if (!groupable) j = i + 1;
+        plan[np++] = Range{i, j - i, groupable && j - i > 1};
+        i = j;
     }
-    const zs_adam no_adam{hp->lr, 0.0, 0.0, 0.0, 0.0};  // the commit's beta^t are unused by SGD
+    // the last launch finishes the step in the control block, then the
+    // restore pass follows; a step with nothing to launch ends in the commit
+    // kernel (its beta^t products are unused by SGD)
+    for (int32_t k = 0; k < np; ++k) {
+        const Range& r = plan[k];
+        zs_ctrl* commit = k + 1 == np ? ctrl_dev : nullptr;
+        const int32_t rc = r.group ? launch_group(shards + r.first, r.count, n_d, width[r.first], *hp, ctrl_dev, commit, st)
+                                   : launch(shards[r.first], n_d, width[r.first], *hp, ctrl_dev, commit, st);
+        if (rc != ZS_OK) return rc;
+    }
+    if (np > 0) return zs::launch_restore_pass(shards, n_shards, ctrl_dev, st);
+    const zs_adam no_adam{hp->lr, 0.0, 0.0, 0.0, 0.0};
     return zs::launch_commit(shards, n_shards, no_adam, ctrl_dev, st);
 }
 

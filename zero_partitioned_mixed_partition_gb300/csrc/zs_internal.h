@@ -63,5 +63,11 @@ uint64_t take_fault_adam8();
 // Enqueues the device-side commit / skip of a step over `shards`.
 int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
                       cudaStream_t stream);
+// Enqueues, with programmatic serialization, the pass that follows a step
+// whose last fused launch already finished it in the control block: it
+// re-casts each shard's fp16 slice from master[cur] if that step overflowed
+// and otherwise leaves at once (shards without a qwZ copy; only params,
+// master and n of each zs_shard are read).
+int32_t launch_restore_pass(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream);
 
 }  // namespace zs
