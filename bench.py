@@ -459,10 +459,12 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
 
     One step is the whole hot path over the stepped shards: the fused
     reduce + overflow test + Adam + fp16 cast launches and the end of the step
-    (for the fp32 Adam, SGD and 8-bit Adam steps, the last fused launch
-    commits and a restore kernel follows that leaves at once unless the step
-    overflowed; the clipped step and a step with a qwZ copy end with the
-    commit kernel).  Returns a dict of the measurements."""
+    (for the fp32 Adam, SGD, 8-bit Adam and clipped steps, the last fused
+    launch commits and a restore kernel follows that leaves at once unless the
+    step overflowed; a step with a qwZ copy ends with the commit kernel).  The
+    per-launch pass of the clipped step calls its two passes one by one, with
+    an event between them and the commit kernel after them.  Returns a dict of
+    the measurements."""
     import torch
     import torch.distributed as dist
     from zero_partitioned_mixed_partition_gb300 import binding
@@ -472,7 +474,14 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
     sgd_hp = binding.sgd(w.lr, 0.9, w.weight_decay)
 
     def one_step(ev=None):
+        if clip and ev is None:
+            # the clipped step's one call: sqnorm cleared, pass 1, pass 2
+            # (its last launch ends the step), then the restore check
+            run.step_clipped(args.clip)
+            return
         if clip:
+            # per-pass times: the same passes called one by one, an event
+            # between them, and the commit kernel after them
             with torch.cuda.stream(stream):
                 run.sqnorm.zero_()
         if ev is not None:
@@ -775,7 +784,7 @@ def main():
         line["qwz"] = {"block": 256, "extra_bytes_per_param": round(1 + 4 / 256, 4)}
     if clip_info is not None:
         line["clip"] = clip_info
-        line["roofline"]["kernel"] = "grad_norm_kernel + clipped_step_kernel + commit_kernel"
+        line["roofline"]["kernel"] = "grad_norm_kernel + clipped_step_kernel + restore_kernel"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         opt = args.optimizer
         ns = oracle_sample(opt, elems)

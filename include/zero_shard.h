@@ -175,8 +175,8 @@ typedef struct zs_ctrl {
     int32_t overflow;      /* OR of the non-finite tests of the step in flight */
     int32_t last_overflow; /* overflow flag of the last finished step */
     uint32_t arrivals;     /* internal block counter of the step's end (the commit kernel, or the
-                              last fused launch of zero_shard_step_async, _sgd_async or
-                              _adam8_async); 0 between steps */
+                              last fused launch of zero_shard_step_async, _sgd_async,
+                              _adam8_async or _clipped_async); 0 between steps */
 } zs_ctrl;
 
 /* ------------------------------------------------------------------------ */
@@ -427,8 +427,11 @@ ZS_API int32_t zero_shard_clipped_adam_all_async(const zs_shard* shards, int32_t
                                                  const double* sqnorm_dev, zs_ctrl* ctrl_dev, void* stream);
 /* Steps 1-4 for shards that all live on this device (the norm is then exact
  * over them): clears *sqnorm_dev, runs pass 1 over every shard, pass 2 over
- * every shard, and the commit.  g_dev: HOST array of n_shards DEVICE
- * pointers (each may be NULL), or NULL to re-reduce everywhere.
+ * every shard, and the commit: without a qwZ copy, pass 2's last launch ends
+ * the step itself and one restore kernel follows (as in
+ * zero_shard_step_async); with one, the commit kernel.  g_dev: HOST array of
+ * n_shards DEVICE pointers (each may be NULL), or NULL to re-reduce
+ * everywhere.
  * Source: "DeepSpeed ZeRO Stages", sec. 2.1, Fact 1 (clipping). */
 ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_shards, int32_t n_d,
                                              const zs_adam* hp, double max_norm, float* const* g_dev,

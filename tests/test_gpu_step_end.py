@@ -185,3 +185,83 @@ def test_all_empty_shards_end_in_the_commit_kernel(zs, oracle, cuda_device, kind
     assert step(live) == 2    # the fused launch, then the restore pass
     c = zs.read_ctrl(ctrl)
     assert c["step"] == 2 and c["cur"] == 0 and c["arrivals"] == 0 and c["last_overflow"] == 0
+
+
+@pytest.mark.parametrize("keep_g", [False, True])
+def test_clipped_back_to_back_equals_the_split_calls(zs, oracle, cuda_device, keep_g):
+    """The clipped step's one call (pass 2's last launch ends the step, then
+    the restore pass; every launch with programmatic serialization), five
+    steps enqueued without host synchronisation over 20 shards (two launches
+    per pass) with an overflow on step 3, against the same steps through the
+    separate pass calls and the commit kernel, synchronised after each step:
+    equal bit for bit, control block included; and the oracle agrees within
+    the stated tolerance."""
+    from zero_partitioned_mixed_partition_gb300.runner import WorkloadRunner
+    from parity_util import OracleShard
+
+    n_d = 20
+    numels = tuple(synth.ragged_numels(70, seed=13, max_exp=12))
+    w = synth.Workload(name="clip-b2b", numels=numels, n_d=n_d, rank=None, align=128, steps=5, lr=1e-3, beta1=0.9,
+                       beta2=0.999, eps=1e-8, weight_decay=0.05, loss_scale=1024.0, grad_dist="normal",
+                       grad_std=1e-2, grad_mult=1024.0, grads_fresh_per_step=False, master_dist="normal",
+                       master_param=0.02, seed=17)
+    a, b = WorkloadRunner(w, cuda_device), WorkloadRunner(w, cuda_device)
+    a.enable_clipping(keep_g)
+    b.enable_clipping(keep_g)
+    victim = a.shard_ids[0]
+    host0 = {r: [synth.fp16_bits(g[: a.n_valid[r]]) for g in a.grads[r]] for r in a.shard_ids}
+    refs = {r: OracleShard(oracle, to_np(a.state[r][0][0][: a.n_valid[r]])) for r in a.shard_ids}
+    sq0 = 0.0
+    for r in a.shard_ids:
+        g, _ = refs[r].reduce(host0[r], w.loss_scale)
+        sq0 = oracle.grad_sqnorm(g, sq0)
+    max_norm = 0.5 * float(np.sqrt(sq0))
+
+    keep = a.grads[victim][2][3].clone()
+    for step in range(1, 6):          # a: no host synchronisation
+        if step == 3:
+            a.grads[victim][2][3] = float("inf")
+        a.step_clipped(max_norm)
+        if step == 3:
+            a.grads[victim][2][3] = keep
+    for step in range(1, 6):          # b: pass by pass, synchronised
+        if step == 3:
+            b.grads[victim][2][3] = float("inf")
+        b.sqnorm.zero_()
+        zs.zero_shard_grad_sqnorm_all_async(b.views, n_d, b.sqnorm, b.ctrl, g_dev=b.gbuf if b.gbuf else None)
+        zs.zero_shard_clipped_adam_all_async(b.views, n_d, b.hp, max_norm, b.sqnorm, b.ctrl,
+                                             g_dev=b.gbuf if b.gbuf else None)
+        zs.zero_step_commit_async(b.views, b.hp, b.ctrl)
+        torch.cuda.synchronize()
+        if step == 3:
+            b.grads[victim][2][3] = keep
+    torch.cuda.synchronize()
+    ca, cb = a.ctrl_host(), b.ctrl_host()
+    assert ca == cb and ca["step"] == 4 and ca["skipped"] == 1 and ca["arrivals"] == 0
+    for r in a.shard_ids:
+        for x, y in zip(a.current(r), b.current(r)):
+            assert torch.equal(x, y), f"shard {r}"
+
+    # the oracle, within the stated tolerance (its norm sums in another order)
+    ls, applied = w.loss_scale, 0
+    for step in range(1, 6):
+        reduced, ovf, sq = [], 0, 0.0
+        for r in a.shard_ids:
+            contribs = [h.copy() for h in host0[r]]
+            if step == 3 and r == victim:
+                contribs[2][3] = 0x7c00
+            g, bad = refs[r].reduce(contribs, ls)
+            reduced.append(g)
+            ovf |= bad
+            sq = oracle.grad_sqnorm(g, sq)
+        c = oracle.clip_factor(sq, max_norm)
+        if not ovf:
+            for r, g in zip(a.shard_ids, reduced):
+                oracle.scale(g, c)
+                refs[r].apply(g, w, applied + 1)
+        ls, applied = oracle.commit(ovf, ls, applied)
+    assert applied == 4 and ca["loss_scale"] == ls
+    for r in a.shard_ids:
+        n = a.n_valid[r]
+        master, m, v, params = a.current(r)
+        refs[r].compare(to_np(master[:n]), to_np(m[:n]), to_np(v[:n]), f16_bits(params[:n]), what=f"shard {r}")

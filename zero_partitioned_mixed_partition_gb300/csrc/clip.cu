@@ -13,7 +13,10 @@
 // Pass 2 either re-reduces the contributions (2 N_d bytes per element) or
 // reads the fp32 g kept by pass 1 (4 bytes, plus 4 written in pass 1); the
 // second is cheaper once N_d > 4.  Per element the clipped step moves
-// 4 N_d + 26 bytes (re-reduce) or 2 N_d + 34 bytes (kept g).
+// 4 N_d + 26 bytes (re-reduce) or 2 N_d + 34 bytes (kept g).  Both passes'
+// launches carry programmatic serialization; in the one-call step without a
+// qwZ copy, pass 2's last launch ends the step in the control block and the
+// restore pass follows, as in the unclipped step.
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -24,6 +27,7 @@
 namespace {
 
 #include "step_common.cuh"
+#include "step_end.cuh"
 
 constexpr int kClipThreads = 256;
 
@@ -51,6 +55,7 @@ struct ClipArgs {
     zs_adam hp;
     const zs_ctrl* ctrl;  // loss scale, t and the ping-pong set
     int32_t* flag;        // &ctrl->overflow
+    zs_ctrl* commit;      // pass 2, non-null: this launch ends the step (arrive_and_finish)
 };
 
 // Block-wide sum of one double per thread; the result is valid in thread 0.
@@ -128,6 +133,8 @@ __device__ __forceinline__ uint32_t norm_elements(const ClipArgs<CAP>& p, int s,
 template <int CAP, int VEC, int ND>
 __global__ void __launch_bounds__(kClipThreads) grad_norm_kernel(const __grid_constant__ ClipArgs<CAP> p) {
     __shared__ float s_inv;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0)
         s_inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)p.n_d, p.ctrl->loss_scale)));
     __syncthreads();
@@ -162,6 +169,8 @@ clipped_step_kernel(const __grid_constant__ ClipArgs<CAP> p) {
     __shared__ Coef s_coef;
     __shared__ float s_clip;
     __shared__ int s_cur;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         const zs_ctrl* ctrl = p.ctrl;
         const double p1 = __dmul_rn(ctrl->beta1_pow, p.hp.beta1);
@@ -210,6 +219,10 @@ clipped_step_kernel(const __grid_constant__ ClipArgs<CAP> p) {
             if (e < p.n[t]) step(std::integral_constant<int, 1>{}, t, e);
         }
     }
+    if (p.commit != nullptr) {   // pass 1 has set the step's flag
+        __syncthreads();
+        if (threadIdx.x == 0) arrive_and_finish(p.commit, gridDim.x, p.hp.beta1, p.hp.beta2);
+    }
 }
 
 // ------------------------------------------------------------ host side ---
@@ -223,10 +236,9 @@ int32_t launch_pass_as(Pass pass, const ClipArgs<CAP>& a, cudaStream_t stream) {
     const int64_t work = a.vstart[a.n_shards];
     const int blocks = zs::persistent_blocks(k, kClipThreads, work > 0 ? work : 1);
     if (pass == Pass::Norm)
-        grad_norm_kernel<CAP, VEC, ND><<<blocks, kClipThreads, 0, stream>>>(a);
-    else
-        clipped_step_kernel<CAP, VEC, ND, FAST><<<blocks, kClipThreads, 0, stream>>>(a);
-    return zs::check_launch(pass == Pass::Norm ? "grad_norm_kernel" : "clipped_step_kernel");
+        return launch_ex(grad_norm_kernel<CAP, VEC, ND>, blocks, kClipThreads, 0, true, stream, a, "grad_norm_kernel");
+    return launch_ex(clipped_step_kernel<CAP, VEC, ND, FAST>, blocks, kClipThreads, 0, true, stream, a,
+                     "clipped_step_kernel");
 }
 
 // ZS_MATH_FAST is taken by the same layouts as in the unclipped step: the
@@ -243,7 +255,8 @@ int32_t launch_pass(Pass pass, const ClipArgs<CAP>& a, cudaStream_t stream) {
 // all of access width `width`; g[i]: shard i's kept-g buffer or nullptr.
 template <int CAP, int ND>
 int32_t launch_cap(Pass pass, const zs_shard* shards, int count, int32_t n_d, int width, float* const* g,
-                   double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+                   double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl, zs_ctrl* commit,
+                   cudaStream_t stream) {
     using Args = ClipArgs<CAP>;
     Args a;
     const bool wide = (ND == 0 || ND > 4) && width == 2 && n_d > 4;
@@ -271,6 +284,7 @@ int32_t launch_cap(Pass pass, const zs_shard* shards, int count, int32_t n_d, in
     a.hp = hp;
     a.ctrl = ctrl;
     a.flag = &ctrl->overflow;
+    a.commit = pass == Pass::Update ? commit : nullptr;
     if constexpr (ND == 0 || ND > 4) {
         if (wide) return launch_pass<CAP, 16, ND>(pass, a, stream);
     }
@@ -282,46 +296,55 @@ int32_t launch_cap(Pass pass, const zs_shard* shards, int count, int32_t n_d, in
 int group_size(int32_t n_d) { return n_d <= 64 ? clip_group<64>() : clip_group<ZS_MAX_ND>(); }
 
 int32_t launch_by_nd(Pass pass, const zs_shard* shards, int count, int32_t n_d, int width, float* const* g,
-                     double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl, cudaStream_t stream) {
+                     double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl, zs_ctrl* commit,
+                     cudaStream_t stream) {
     switch (n_d) {
-    case 16: return launch_cap<16, 16>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    case 32: return launch_cap<32, 32>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    case 64: return launch_cap<64, 64>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    case 16: return launch_cap<16, 16>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, commit, stream);
+    case 32: return launch_cap<32, 32>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, commit, stream);
+    case 64: return launch_cap<64, 64>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, commit, stream);
     default: break;
     }
-    if (n_d <= 4) return launch_cap<4, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    if (n_d <= 16) return launch_cap<16, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    if (n_d <= 64) return launch_cap<64, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
-    return launch_cap<ZS_MAX_ND, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, stream);
+    if (n_d <= 4) return launch_cap<4, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, commit, stream);
+    if (n_d <= 16) return launch_cap<16, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, commit, stream);
+    if (n_d <= 64) return launch_cap<64, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, commit, stream);
+    return launch_cap<ZS_MAX_ND, 0>(pass, shards, count, n_d, width, g, sqnorm, max_norm, hp, ctrl, commit, stream);
 }
 
 // Pass 1 or 2 for shards[0, n_shards): consecutive non-empty shards of one
 // access width share a launch (up to the group size); after pass 2 each
 // shard's qwZ copy (if any) is rebuilt from its new fp16 slice in its own pass
-// (3 + 4/256 bytes per element).
+// (3 + 4/256 bytes per element).  commit (pass 2 only): given to the last
+// launch, which then ends the step; *launched says whether anything ran.
 int32_t launch_all(Pass pass, const zs_shard* shards, int32_t n_shards, int32_t n_d, const int* width,
                    float* const* g, double* sqnorm, double max_norm, const zs_adam& hp, zs_ctrl* ctrl,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, zs_ctrl* commit = nullptr, bool* launched = nullptr) {
     const int gmax = group_size(n_d);
-    int32_t i = 0;
+    struct Range { int32_t first, count; };
+    Range plan[ZS_MAX_SHARDS];
+    int32_t np = 0, i = 0;
     while (i < n_shards) {
         if (shards[i].n == 0) { ++i; continue; }
         int32_t j = i + 1;
         while (j < n_shards && j - i < gmax && width[j] == width[i] && shards[j].n > 0) ++j;
-        int32_t rc = launch_by_nd(pass, shards + i, j - i, n_d, width[i], g ? g + i : nullptr, sqnorm, max_norm, hp,
-                                  ctrl, stream);
+        plan[np++] = Range{i, j - i};
+        i = j;
+    }
+    for (int32_t k = 0; k < np; ++k) {
+        const int32_t first = plan[k].first, last = first + plan[k].count;
+        int32_t rc = launch_by_nd(pass, shards + first, plan[k].count, n_d, width[first], g ? g + first : nullptr,
+                                  sqnorm, max_norm, hp, ctrl, k + 1 == np ? commit : nullptr, stream);
         if (rc != ZS_OK) return rc;
         if (pass == Pass::Update) {
-            for (int32_t k = i; k < j; ++k) {
-                const zs_shard& s = shards[k];
+            for (int32_t q = first; q < last; ++q) {
+                const zs_shard& s = shards[q];
                 if (s.qcodes == nullptr) continue;
                 rc = zs::launch_qwz(nullptr, s.params, s.n, s.qcodes, s.qscales, 0, (s.n + kQwzBlock - 1) / kQwzBlock,
                                     stream);
                 if (rc != ZS_OK) return rc;
             }
         }
-        i = j;
     }
+    if (launched) *launched = np > 0;
     return ZS_OK;
 }
 
@@ -407,8 +430,16 @@ ZS_API int32_t zero_shard_step_clipped_async(const zs_shard* shards, int32_t n_s
     const zs_adam none{0.0, 0.0, 0.0, 0.0, 0.0, 0, 0};
     rc = launch_all(Pass::Norm, shards, n_shards, n_d, width, g_dev, sqnorm_dev, 0.0, none, ctrl_dev, st);
     if (rc != ZS_OK) return rc;
-    rc = launch_all(Pass::Update, shards, n_shards, n_d, width, g_dev, sqnorm_dev, max_norm, *hp, ctrl_dev, st);
+    // Without a qwZ copy, pass 2's last launch ends the step in the control
+    // block and the restore pass follows; with one (rebuilt after pass 2), or
+    // with nothing launched, the commit kernel ends it.
+    bool any_qwz = false;
+    for (int32_t i = 0; i < n_shards; ++i) any_qwz |= shards[i].qcodes != nullptr;
+    bool launched = false;
+    rc = launch_all(Pass::Update, shards, n_shards, n_d, width, g_dev, sqnorm_dev, max_norm, *hp, ctrl_dev, st,
+                    any_qwz ? nullptr : ctrl_dev, &launched);
     if (rc != ZS_OK) return rc;
+    if (!any_qwz && launched) return zs::launch_restore_pass(shards, n_shards, ctrl_dev, st);
     return zs::launch_commit(shards, n_shards, *hp, ctrl_dev, st);
 }
 
