@@ -436,6 +436,8 @@ template <int MAXS>
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ CommitArgs<MAXS> p) {
     __shared__ int s_ovf, s_cur;
     zs_ctrl* ctrl = p.ctrl;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         s_ovf = *reinterpret_cast<volatile int32_t*>(&ctrl->overflow);
         s_cur = *reinterpret_cast<volatile int32_t*>(&ctrl->cur);
@@ -678,10 +680,10 @@ int32_t launch_commit_cap(const zs_shard* shards, int32_t n_shards, const zs_ada
     a.beta2 = hp.beta2;
     a.ctrl = ctrl;
     // one block per SM: enough to restore the slices at full bandwidth on an
-    // overflow step, few enough that a normal step costs only the arrivals
+    // overflow step, few enough that a normal step costs only the arrivals;
+    // programmatic serialization, as the fused launches
     const int blocks = zs::device_sm_count();
-    commit_kernel<MAXS><<<blocks, kCommitThreads, 0, stream>>>(a);
-    return zs::check_launch("commit_kernel");
+    return launch_ex(commit_kernel<MAXS>, blocks, kCommitThreads, 0, true, stream, a, "commit_kernel");
 }
 
 int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& hp, zs_ctrl* ctrl,
@@ -1172,13 +1174,14 @@ ZS_API int32_t zero_shard_step_async(const zs_shard* shards, int32_t n_shards, i
     cudaStream_t st = (cudaStream_t)stream;
     // Without a qwZ copy the step's last fused launch finishes the step in the
     // control block itself and a restore pass follows (it leaves at once unless
-    // the step overflowed), both with programmatic serialization; with one,
-    // the commit kernel also writes the qwZ copies' trailing blocks.
+    // the step overflowed); with one, the commit kernel ends the step and also
+    // writes the qwZ copies' trailing blocks.  Every launch carries
+    // programmatic serialization.
     bool any_qwz = false;
     for (int32_t i = 0; i < n_shards; ++i) any_qwz |= shards[i].qcodes != nullptr;
     LaunchOpts o;
     o.commit = any_qwz ? nullptr : ctrl_dev;
-    o.pdl = !any_qwz;
+    o.pdl = true;
     bool committed = false;
     rc = launch_steps(shards, n_shards, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, false, o,
                       &committed, st);
@@ -1194,8 +1197,10 @@ ZS_API int32_t zero_shard_reduce_adam_all_async(const zs_shard* shards, int32_t 
     int width[ZS_MAX_SHARDS];
     int32_t rc = check_shard_list(shards, n_shards, n_d, width);
     if (rc != ZS_OK) return rc;
-    return launch_steps(shards, n_shards, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, false,
-                        LaunchOpts{}, nullptr, (cudaStream_t)stream);
+    LaunchOpts o;
+    o.pdl = true;   // the commit kernel that ends this split form waits for them
+    return launch_steps(shards, n_shards, n_d, width, nullptr, 0, *hp, ctrl_dev, &ctrl_dev->overflow, false, o,
+                        nullptr, (cudaStream_t)stream);
 }
 
 // Device-usable address of page-locked, mapped host memory (nullptr if the
