@@ -373,8 +373,10 @@ def offload_throughput(run, w, n_sample: int, steps: int, threads: int):
     the first n_sample parameters of the rank's shard: the contributions come
     from the runner's device buffers, the fp32 state lives in host memory, the
     fp16 parameters go to a device buffer; two CUDA streams for the two link
-    directions.  Wall-clock per synchronous step after one untimed step.
-    Returns a dict for the JSON line."""
+    directions.  Wall-clock of each synchronous step after one untimed step;
+    the rate is taken from the median step (the host threads share the cores
+    with the rest of the machine, so single steps vary).  Returns a dict for
+    the JSON line."""
     import torch
     from zero_partitioned_mixed_partition_gb300 import binding, synth
     r = run.shard_ids[0]
@@ -391,18 +393,19 @@ def offload_throughput(run, w, n_sample: int, steps: int, threads: int):
     hp = binding.adam(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     d2h, h2d = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
-    cur = 0
+    cur, times = 0, []
     for k in range(steps + 1):
-        if k == 1:
-            t0 = time.perf_counter()
+        t0 = time.perf_counter()
         ovf = binding.zero_shard_step_offload(view, w.n_d, hp, w.loss_scale, k + 1, cur, n_threads=threads,
                                               d2h_stream=d2h, h2d_stream=h2d)
+        if k > 0:
+            times.append((time.perf_counter() - t0) * 1e3)
         assert ovf == 0
         cur ^= 1
-    el = time.perf_counter() - t0
-    ms = el / steps * 1e3
+    ms = statistics.median(times)
     d2h_b, h2d_b = 2 * w.n_d * n, 2 * n
     return {"value": round(n / (ms / 1e3) / 1e9, 4), "unit": "Gparams/s", "ms_per_step": round(ms, 3),
+            "ms_min_max": [round(min(times), 3), round(max(times), 3)],
             "shard_params": n, "cores": threads, "steps": steps,
             "link_bytes_per_step": {"d2h": d2h_b, "h2d": h2d_b},
             "link_gbs": {"d2h": round(d2h_b / (ms / 1e3) / 1e9, 1), "h2d": round(h2d_b / (ms / 1e3) / 1e9, 1)},
@@ -828,7 +831,7 @@ def main():
                               "host_copy_gbs": round(ceiling, 1),
                               "frac_of_host_copy": round(g * step_bytes_per_param("adam", w.n_d) / ceiling, 3)}
         if not args.no_offload:
-            line["offload"] = offload_throughput(run, w, args.offload_params, 3, th)
+            line["offload"] = offload_throughput(run, w, args.offload_params, 10, th)
 
     # the other target configurations of the same step, each on its own
     # buffers after the previous ones are freed, timed the same way
