@@ -335,7 +335,6 @@ ZS_API int32_t zero_shard_step_sgd_async(const zs_shard* shards, int32_t n_shard
         int32_t j = i + 1;
         if (groupable)
             while (j < n_shards && j - i < kSgdGroupMax && width[j] == width[i]) ++j;
-        if (!groupable) j = i + 1;
         plan[np++] = Range{i, j - i, groupable && j - i > 1};
         i = j;
     }
