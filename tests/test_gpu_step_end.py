@@ -265,3 +265,58 @@ def test_clipped_back_to_back_equals_the_split_calls(zs, oracle, cuda_device, ke
         n = a.n_valid[r]
         master, m, v, params = a.current(r)
         refs[r].compare(to_np(master[:n]), to_np(m[:n]), to_np(v[:n]), f16_bits(params[:n]), what=f"shard {r}")
+
+
+@pytest.mark.parametrize("kind", ["sgd", "adam8", "clip"])
+def test_graph_captured_steps_of_each_kind(zs, cuda_device, kind):
+    """Two steps of each kind captured in one CUDA graph (their launches carry
+    programmatic serialization, so the graph holds programmatic edges) and
+    replayed three times equal six steps run eagerly on a twin, bit for bit,
+    control block included; 20 shards, so each step is two grouped launches
+    and the restore pass."""
+    from zero_partitioned_mixed_partition_gb300.runner import WorkloadRunner
+
+    numels = tuple(synth.ragged_numels(70, seed=19, max_exp=12))
+    w = synth.Workload(name="graph", numels=numels, n_d=20, rank=None, align=128, steps=6, lr=1e-3, beta1=0.9,
+                       beta2=0.999, eps=1e-8, weight_decay=0.05, loss_scale=1024.0, grad_dist="normal",
+                       grad_std=1e-2, grad_mult=1024.0, grads_fresh_per_step=False, master_dist="normal",
+                       master_param=0.02, seed=23)
+    a, b = WorkloadRunner(w, cuda_device), WorkloadRunner(w, cuda_device)
+    hp = zs.sgd(LR, MU, WD)
+    for run in (a, b):
+        if kind == "adam8":
+            run.enable_adam8()
+        if kind == "clip":
+            run.enable_clipping(True)
+    max_norm = 0.05
+
+    def step(run):
+        if kind == "sgd":
+            run.step_sgd(hp)
+        elif kind == "adam8":
+            run.step_adam8()
+        else:
+            run.step_clipped(max_norm)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(a)                                    # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(a)
+        step(a)
+    for _ in range(3):
+        g.replay()
+    for _ in range(7):
+        step(b)
+    torch.cuda.synchronize()
+    ca, cb = a.ctrl_host(), b.ctrl_host()
+    assert ca == cb and ca["step"] == 7 and ca["skipped"] == 0 and ca["arrivals"] == 0
+    for r in a.shard_ids:
+        sa = a.current_adam8(r) if kind == "adam8" else a.current(r)
+        sb = b.current_adam8(r) if kind == "adam8" else b.current(r)
+        for x, y in zip(sa, sb):
+            assert torch.equal(x, y), f"{kind} shard {r}"
