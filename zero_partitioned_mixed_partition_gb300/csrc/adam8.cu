@@ -675,7 +675,7 @@ ZS_API int32_t zero_shard_step_adam8_async(const zs_adam8_shard* shards, int32_t
         ends[s].params = shards[s].params;
         ends[s].n = shards[s].n;
     }
-    if (np > 0) return zs::launch_restore_pass(ends, n_shards, ctrl_dev, st);
+    if (np > 0) return zs::launch_restore_pass(ends, n_shards, ctrl_dev, st, true);
     return zs::launch_commit(ends, n_shards, *hp, ctrl_dev, st);  // nothing launched: the commit kernel ends it
 }
 

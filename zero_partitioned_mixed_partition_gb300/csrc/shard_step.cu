@@ -345,6 +345,7 @@ template <int MAXS>
 struct CommitArgs {
     CommitShard shards[MAXS];
     int32_t n_shards;
+    int32_t early_dependents;  // restore pass: let the next kernel be scheduled before waiting
     double beta1, beta2;
     zs_ctrl* ctrl;
 };
@@ -469,12 +470,20 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
 // otherwise every block leaves at once.  Shards with a qwZ copy do not take
 // this path.  Launched with programmatic serialization, so its launch overlaps
 // the end of the fused kernel; it reads the control block only after that
-// kernel has completed.
+// kernel has completed.  With early_dependents it lets the next kernel of the
+// stream be scheduled before it waits (that kernel's own wait still covers
+// this one's completion): the 8-bit Adam kernel then copies its code tables
+// while the step ahead drains.
 template <int MAXS>
 __global__ void __launch_bounds__(kCommitThreads) restore_kernel(const __grid_constant__ CommitArgs<MAXS> p) {
     __shared__ int s_ovf, s_cur;
-    griddep_wait();
-    griddep_launch_dependents();
+    if (p.early_dependents) {
+        griddep_launch_dependents();
+        griddep_wait();
+    } else {
+        griddep_wait();
+        griddep_launch_dependents();
+    }
     if (threadIdx.x == 0) {
         s_ovf = *reinterpret_cast<volatile int32_t*>(&p.ctrl->last_overflow);
         s_cur = *reinterpret_cast<volatile int32_t*>(&p.ctrl->cur);
@@ -676,6 +685,7 @@ int32_t launch_commit_cap(const zs_shard* shards, int32_t n_shards, const zs_ada
         }
     }
     a.n_shards = n_shards;
+    a.early_dependents = 0;
     a.beta1 = hp.beta1;
     a.beta2 = hp.beta2;
     a.ctrl = ctrl;
@@ -942,7 +952,8 @@ int32_t launch_steps(const zs_shard* shards, int32_t n_shards, int32_t n_d, cons
 // The restore pass after a step that a fused launch finished (restore_kernel),
 // with programmatic serialization.
 template <int MAXS>
-int32_t launch_restore_cap(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream) {
+int32_t launch_restore_cap(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, bool early,
+                           cudaStream_t stream) {
     CommitArgs<MAXS> a;
     for (int i = 0; i < MAXS; ++i) {
         if (i < n_shards)
@@ -952,6 +963,7 @@ int32_t launch_restore_cap(const zs_shard* shards, int32_t n_shards, zs_ctrl* ct
             a.shards[i] = CommitShard{nullptr, {nullptr, nullptr}, 0, nullptr, nullptr};
     }
     a.n_shards = n_shards;
+    a.early_dependents = early ? 1 : 0;
     a.beta1 = 0.0;
     a.beta2 = 0.0;
     a.ctrl = ctrl;
@@ -960,18 +972,20 @@ int32_t launch_restore_cap(const zs_shard* shards, int32_t n_shards, zs_ctrl* ct
                          "restore_kernel");
 }
 
-int32_t launch_restore(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream) {
-    if (n_shards <= 1) return launch_restore_cap<1>(shards, n_shards, ctrl, stream);
-    if (n_shards <= 16) return launch_restore_cap<16>(shards, n_shards, ctrl, stream);
-    return launch_restore_cap<ZS_MAX_SHARDS>(shards, n_shards, ctrl, stream);
+int32_t launch_restore(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream,
+                       bool early = false) {
+    if (n_shards <= 1) return launch_restore_cap<1>(shards, n_shards, ctrl, early, stream);
+    if (n_shards <= 16) return launch_restore_cap<16>(shards, n_shards, ctrl, early, stream);
+    return launch_restore_cap<ZS_MAX_SHARDS>(shards, n_shards, ctrl, early, stream);
 }
 
 }  // namespace
 
 namespace zs {
 uint64_t take_fault_shard_step() { return take_fault(); }
-int32_t launch_restore_pass(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream) {
-    return launch_restore(shards, n_shards, ctrl, stream);
+int32_t launch_restore_pass(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream,
+                            bool early_dependents) {
+    return launch_restore(shards, n_shards, ctrl, stream, early_dependents);
 }
 }  // namespace zs
 

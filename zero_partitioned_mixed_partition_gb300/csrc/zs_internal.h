@@ -67,7 +67,11 @@ int32_t launch_commit(const zs_shard* shards, int32_t n_shards, const zs_adam& h
 // whose last fused launch already finished it in the control block: it
 // re-casts each shard's fp16 slice from master[cur] if that step overflowed
 // and otherwise leaves at once (shards without a qwZ copy; only params,
-// master and n of each zs_shard are read).
-int32_t launch_restore_pass(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream);
+// master and n of each zs_shard are read).  early_dependents: let the next
+// kernel of the stream be scheduled before this pass waits (measured faster
+// ahead of the 8-bit Adam kernel, whose CTAs first copy their code tables,
+// and slower ahead of the fp32 Adam and SGD kernels).
+int32_t launch_restore_pass(const zs_shard* shards, int32_t n_shards, zs_ctrl* ctrl, cudaStream_t stream,
+                            bool early_dependents = false);
 
 }  // namespace zs
