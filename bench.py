@@ -64,6 +64,10 @@ def parse_args():
                          "(8-bit Adam: m, v as 8-bit codes with a scale per 2048 elements)")
     ap.add_argument("--qwz", action="store_true",
                     help="keep the int8 qwZ copy of the fp16 shard in each step (1 + 4/256 bytes per element)")
+    ap.add_argument("--api", default="async", choices=["async", "sync", "noalloc"],
+                    help="entry point of the fp32 Adam step: zero_shard_step_async (device commit, no host "
+                         "sync), zero_shard_step (flag buffer, host sync and commit per step) or "
+                         "zero_shard_step_noalloc (as zero_shard_step, flag words inside the library)")
     ap.add_argument("--math", default="fast", choices=["fast", "ieee"],
                     help="rounding of the Adam update's last division: fast (ZS_MATH_FAST, corrected hardware "
                          "reciprocal, within 1 ulp) or ieee (every operation IEEE, bit-exact)")
@@ -98,6 +102,17 @@ def workload(args):
     return w
 
 
+def step_api_name(args) -> str:
+    """The C-ABI entry point one timed step calls."""
+    opt = getattr(args, "optimizer", "adam")
+    if opt != "adam":
+        return f"zero_shard_step_{opt}_async"
+    if getattr(args, "clip", 0.0) > 0:
+        return "zero_shard_step_clipped_async"
+    return {"async": "zero_shard_step_async", "sync": "zero_shard_step",
+            "noalloc": "zero_shard_step_noalloc"}[getattr(args, "api", "async")]
+
+
 def arm_config(args, w, elems: int, bytes_step: int, world: int) -> dict:
     """The workload description both arms print (the reference arm times a
     bounded sample of this same workload and says so in its cpu_baseline)."""
@@ -107,6 +122,7 @@ def arm_config(args, w, elems: int, bytes_step: int, world: int) -> dict:
                         "adam8": "fp16 grads and params, fp32 master, 8-bit m/v codes + fp32 scale per 2048 "
                                  "(ping-pong)"}.get(getattr(args, "optimizer", "adam"),
                                                    "fp16 grads and params, fp32 master/m/v (ping-pong)"),
+            "api": step_api_name(args),
             "math": ("ZS_MATH_FAST: u by corrected hardware reciprocal (within 1 ulp), all else IEEE; "
                      "m/v bit-exact" if args.math == "fast" else "ZS_MATH_IEEE: every fp32 operation IEEE, "
                      "bit-exact"),
@@ -495,6 +511,26 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
 
     clip = args.clip > 0
     sgd_hp = binding.sgd(w.lr, 0.9, w.weight_decay)
+    api = getattr(args, "api", "async")
+    # the synchronous entry points take the loss scale, t and the state set
+    # from the caller, who commits or skips after each step (kept here)
+    host = run.ctrl_host()
+    hstate = {"ls": host["loss_scale"], "t": host["step"] + 1, "cur": host["cur"], "applied": 0}
+    flag_dev = torch.zeros(1, dtype=torch.int32, device=run.device) if api == "sync" else None
+
+    def sync_step():
+        if api == "sync":
+            ovf = binding.zero_shard_step(run.views, w.n_d, run.hp, hstate["ls"], hstate["t"], hstate["cur"],
+                                          flag_dev, stream=stream)
+        else:
+            ovf = binding.zero_shard_step_noalloc(run.views, w.n_d, run.hp, hstate["ls"], hstate["t"],
+                                                  hstate["cur"], stream=stream)
+        if ovf:
+            hstate["ls"] = max(hstate["ls"] / 2, 1.0)
+        else:
+            hstate["cur"] ^= 1
+            hstate["t"] += 1
+            hstate["applied"] += 1
 
     def one_step(ev=None):
         if clip and ev is None:
@@ -513,6 +549,8 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
             run.step_sgd(sgd_hp)      # fused kernel(s) ending the step, then the restore check
         elif args.optimizer == "adam8":
             run.step_adam8()          # fused kernel(s) ending the step, then the restore check
+        elif not clip and api != "async":
+            sync_step()               # fused kernel(s), host sync, commit kept on the host
         elif not clip:
             run.step()                # fused kernel(s) ending the step, then the restore check
         else:
@@ -572,7 +610,10 @@ def time_steps(args, run, w, stream, world, steps, warmup, prewarm_s, local):
         out["norm_ms"] = [ev[0].elapsed_time(ev[2]) for ev in pairs]
         out["upd_ms"] = [ev[2].elapsed_time(ev[1]) for ev in pairs]
     ctrl = run.ctrl_host()
-    assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + warmup + 2 * steps, ctrl
+    if api == "async" or clip or args.optimizer != "adam":
+        assert ctrl["skipped"] == 0 and ctrl["step"] == prewarm_steps + warmup + 2 * steps, ctrl
+    else:
+        assert hstate["applied"] == prewarm_steps + warmup + 2 * steps, hstate
     out["ctrl"] = ctrl
     out["ms_max"] = zdist.max_over_ranks(ms_total, device=torch.device("cuda", local))
     return out
@@ -691,6 +732,8 @@ def main():
     clip = args.clip > 0
     if args.optimizer != "adam" and (clip or args.qwz):
         raise SystemExit(f"--optimizer {args.optimizer} goes without --clip / --qwz")
+    if args.api != "async" and (args.optimizer != "adam" or clip):
+        raise SystemExit("--api sync|noalloc times the fp32 Adam step without --clip")
     if args.optimizer == "adam8":
         run.enable_adam8()
     if clip:
