@@ -16,7 +16,12 @@
 // shard and walks it in tiles of kTile elements; per tile the contributions
 // are summed contribution by contribution into a tile accumulator (the inner
 // loop runs over elements, so the compiler vectorises it), then the update
-// runs over the tile.  Rank order per element is kept.
+// runs over the tile.  Rank order per element is kept.  The step is bound by
+// how fast one core streams its eleven arrays (with every division and the
+// square root replaced by multiplies it ran only 4 % faster on 16 Grace
+// cores), and longer runs per array stream faster: 65,536-element tiles (the
+// accumulator, 256 KB, stays in the core's L2) measured 5.34-5.49 Gparams/s
+// on 16 Grace cores against 4.80-4.85 with 2,048-element tiles.
 #include <stdint.h>
 #include <string.h>
 
@@ -35,7 +40,8 @@
 
 namespace {
 
-constexpr int64_t kTile = 2048;
+constexpr int64_t kTile = 65536;
+constexpr int64_t kMinThreadChunk = 2048;  // below 2 x this many elements one thread steps them all
 
 struct CpuCoef {
     float b1, c1, b2, c2, bc1, bc2, lr, eps, wd, inv;
@@ -117,7 +123,8 @@ void update_tile(typename TilePtrs<RESTRICT>::CF acc, typename TilePtrs<RESTRICT
 
 // Steps [lo, hi) of the shard; returns 1 if a reduced gradient was not finite.
 int step_chunk(const zs_shard& s, int n_d, const CpuCoef& c, int cur, int64_t lo, int64_t hi) {
-    float acc[kTile];
+    std::unique_ptr<float[]> accbuf(new float[(size_t)std::max<int64_t>(1, std::min(kTile, hi - lo))]);
+    float* acc = accbuf.get();
     int bad = 0;
     const float* th_in = s.master[cur];
     const float* m_in = s.m[cur];
@@ -152,7 +159,7 @@ void restore_chunk(const zs_shard& s, int cur, int64_t lo, int64_t hi) {
 
 template <typename F>
 void parallel_chunks(int64_t n, int threads, F&& f) {
-    if (threads <= 1 || n < 2 * kTile) {
+    if (threads <= 1 || n < 2 * kMinThreadChunk) {
         f(0, (int64_t)0, n);
         return;
     }
