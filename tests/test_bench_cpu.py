@@ -76,3 +76,18 @@ def test_reference_arm_line(optimizer):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["config"]["bytes_per_param"] == round(bench.step_bytes_per_param(optimizer, 4), 4)
     assert optimizer in line["cpu_baseline"]["sample"]
+
+
+def test_step_api_names():
+    """The config of every line names the C-ABI entry point one timed step calls."""
+    import argparse
+    def ns(**kw):
+        base = dict(optimizer="adam", clip=0.0, api="async")
+        base.update(kw)
+        return argparse.Namespace(**base)
+    assert bench.step_api_name(ns()) == "zero_shard_step_async"
+    assert bench.step_api_name(ns(api="sync")) == "zero_shard_step"
+    assert bench.step_api_name(ns(api="noalloc")) == "zero_shard_step_noalloc"
+    assert bench.step_api_name(ns(clip=1.0)) == "zero_shard_step_clipped_async"
+    assert bench.step_api_name(ns(optimizer="sgd")) == "zero_shard_step_sgd_async"
+    assert bench.step_api_name(ns(optimizer="adam8")) == "zero_shard_step_adam8_async"
