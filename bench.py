@@ -82,7 +82,7 @@ def parse_args():
                     help="skip the ZeRO-Offload step (device -> host -> device) measurement")
     ap.add_argument("--offload-params", type=int, default=96_000_000,
                     help="parameters of the rank's shard the ZeRO-Offload measurement steps")
-    ap.add_argument("--extra-configs", default="7b5,gpt2s",
+    ap.add_argument("--extra-configs", default="7b5,gpt2s,ragged",
                     help="other workloads timed in the same run after the main one (fp32 Adam step only), "
                          "reported under 'configs'; '' for none")
     return ap.parse_args()
